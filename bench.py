@@ -1,0 +1,317 @@
+"""Benchmark of the codebook-quantized MoE FFN hot path on GB300.
+
+Default workload: batch-1 decode of one MoE FFN layer (hidden 4096, expert
+intermediate 2048, 256 routed experts, top-6 + an always-on shared expert;
+routed gate/up FP2, routed down FP3, shared expert FP4, bf16 router). One step
+decodes one token through moe_ffn_decode (one persistent kernel). Steps cycle
+through independently seeded layer replicas (default 8 x 2.3 GB) so that no
+step finds its weights in the 129 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0). Under torchrun every rank decodes its own token
+stream on its own GPU (independent problems, no data-path collective): weak
+scaling; value = all ranks' tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = ("decode-b1: H=4096 I=2048 E=256 top-6 + shared expert; routed gate/up FP2 (10 B/32), "
+            "routed down FP3 (14 B/32), shared FP4 (17 B/32), bf16 router")
+CFG_ID = 1
+
+
+def algorithmic_bytes_decode(cfg: dict) -> int:
+    """Packed weight bytes one token reads: router + k routed experts + shared expert."""
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["k"]
+    per_blk = {2: 10, 3: 14, 4: 17}
+    routed = 2 * I * (H // 32) * per_blk[cfg["fmt_gu"]] + H * (I // 32) * per_blk[cfg["fmt_down"]]
+    shared = 0
+    if cfg["shared_fmt"]:
+        shared = 3 * I * (H // 32) * per_blk[cfg["shared_fmt"]]
+    return E * H * 2 + k * routed + shared
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def _traffic(kernel: str, source: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    with open(os.path.join(ROOT, source), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return ent["bytes_per_launch"] if ent.get("source_sha") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moeq_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline(cfg_id: int, tokens: int, seconds_cap: float = 30.0):
+    """The oracle, as it stands, timed on this host (one core) on a bounded
+    sample of the workload's tokens. Returns (tokens/s, sample description)."""
+    import oracle as O
+    from oracle import workload as W
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    cfg = S.CONFIGS[cfg_id]
+    seed = S.config_seed(cfg_id)
+    xs = S.tokens(seed, cfg, tokens)
+    experts = set()
+    wr = S.router_weights(seed, 0, cfg)
+    lg = O.router_logits(xs, wr)
+    for t in range(tokens):
+        experts.update(int(e) for e in O.topk(lg[t], cfg["k"])[0])
+    L = W.layer(seed, 0, cfg, experts)
+    done = 0
+    t0 = time.perf_counter()
+    for t in range(tokens):
+        O.ffn_decode(L, xs[t])
+        done += 1
+        if time.perf_counter() - t0 > seconds_cap:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, f"{done} tokens of the decode workload (layer 0), oracle single-threaded", dt
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    tps, sample, dt = cpu_baseline(CFG_ID, max(1, min(args.steps, 4)))
+    line = {"impl": "reference", "metric": "MoE-FFN decode tok/s", "value": tps,
+            "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 / tps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": tps, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": tps, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run(args):
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, to_dev_u16
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = S.CONFIGS[CFG_ID]
+    seed = S.config_seed(CFG_ID)
+    M.load()
+    R = args.replicas
+    layers = [build_layer(seed, r, cfg) for r in range(R)]
+    wss = [Workspace(dl, 0) for dl in layers]
+    ntok = 1024
+    xs_host = S.tokens(seed, cfg, ntok, start=rank * ntok)
+    xs = to_dev_u16(xs_host)                      # [ntok, H] resident in HBM
+    H = cfg["H"]
+    y = torch.zeros(H, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    descs = [dl.desc() for dl in layers]
+    stream = torch.cuda.current_stream()
+    xbase, xstride = xs.data_ptr(), H * 2
+
+    def step(i):
+        r = i % R
+        M.moe_ffn_decode(descs[r], xbase + (i % ntok) * xstride, y, wss[r].ptr, wss[r].nbytes, st,
+                         None, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    assert st.item() == 0, f"device status {st.item()}"
+
+    # end to end through the same entry point with host buffers: pinned x in,
+    # y out, both inside the timed region
+    x_pin = torch.from_numpy(xs_host.view(np.int16)).pin_memory()
+    y_pin = torch.empty((args.steps, H), dtype=torch.float32).pin_memory()
+    xdev = torch.empty(H, dtype=torch.int16, device="cuda")
+
+    def step_e2e(i):
+        r = i % R
+        xdev.copy_(x_pin[i % ntok], non_blocking=True)
+        M.moe_ffn_decode(descs[r], xdev, y, wss[r].ptr, wss[r].nbytes, st, None, stream)
+        y_pin[i % args.steps].copy_(y, non_blocking=True)
+
+    for i in range(args.warmup):
+        step_e2e(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step_e2e(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+
+    if dist:
+        t = torch.tensor([ms, ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    hbm_peak, _, peak_kind = _peaks()
+    per_tok = algorithmic_bytes_decode(cfg)
+    ms_step = ms / args.steps
+    achieved = per_tok / (ms_step * 1e-3) / 1e9
+    value = world * args.steps / (ms * 1e-3)
+    e2e = world * args.steps / (ms_e2e * 1e-3)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tps, sample, _ = cpu_baseline(CFG_ID, 20)
+        cpu = {"value": tps, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample}
+    traffic = _traffic("decode_kernel", "bit_codebook_quantized_dequant_gb300/csrc/decode.cu")
+    line = {
+        "metric": "MoE-FFN decode tok/s (batch 1, one layer)",
+        "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8-dot/fp32",
+        "data": "synthetic (seeded SplitMix64 codes, scales, codebooks; x ~ N(0,1) bf16)",
+        "config": {"workload": WORKLOAD, "replicas": R,
+                   "l2": f"inputs larger than L2: {R} independently seeded layer replicas "
+                         f"({R * layers[0].weight_bytes() / 1e9:.1f} GB), cycled per step",
+                   "tokens": ntok},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": per_tok},
+        "gpu_launches": args.steps,
+        "e2e": {"value": e2e, "unit": "tok/s", "h2d_bytes_per_step": H * 2,
+                "d2h_bytes_per_step": H * 4},
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--replicas", type=int, default=8)
+    ap.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,347 @@
+// Device helpers of the moeq CUDA library (sm_103a): PTX wrappers for
+// mbarriers, bulk async copies and ordered global accesses; codebook expansion
+// of FP2/FP3/FP4 blocks with byte permutes and int8 dot products; the Q8
+// activation quantizer; the H32 rotation. Layouts are those of include/moeq.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "moeq.h"
+
+namespace moeq {
+
+constexpr int kMaxK = 8;                 // top-k limit of the fused kernels
+constexpr uint32_t kSpinLimit = 1u << 20;  // bounded waits: well under a second each
+
+// ------------------------------------------------------------------ status
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 16) __nanosleep(64);
+  }
+  return false;
+}
+
+// Bulk asynchronous copy global -> shared (size and both addresses multiples of 16).
+__device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded spin until *p >= target (acquire). false when the limit ran out.
+__device__ __forceinline__ bool spin_until_geq(const uint32_t* p, uint32_t target) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (ld_acquire(p) >= target) return true;
+    if (i > 8) __nanosleep(64);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier that also returns the AND of pred over the participating threads.
+__device__ __forceinline__ bool named_bar_and(int id, int threads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return out != 0;
+}
+
+// ------------------------------------------------------------------ small conversions
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t b) {
+  return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ float e8m0_to_f32(uint8_t e) {
+  // 2^(e-127); e = 0 gives 2^-127 (a subnormal float), e = 255 is rejected upstream
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(e) << 23);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+  uint32_t x = __float_as_uint(f);
+  if ((x & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((x >> 16) | 0x40u);
+  x += 0x7fffu + ((x >> 16) & 1u);
+  return static_cast<uint16_t>(x >> 16);
+}
+
+// ------------------------------------------------------------------ codebook expansion
+// Block dot products S = sum_j cb[code_j] * q_j for one 32-weight block against
+// 32 int8 activations packed little-endian in q[0..7] (q[i] = elements 4i..4i+3).
+// The codebook sits in registers; byte permutes expand four codes per
+// instruction, dp4a multiplies and accumulates four products.
+
+// FP2: cb = entries 0..3 in one word; w0, w1 the block's words.
+__device__ __forceinline__ int dot_fp2(uint32_t w0, uint32_t w1, uint32_t cb, const int* q) {
+  uint32_t a = w0 & 0x33333333u, b = (w0 >> 2) & 0x33333333u;
+  int s = __dp4a(static_cast<int>(prmt(cb, cb, a)), q[0], 0);
+  s = __dp4a(static_cast<int>(prmt(cb, cb, a >> 16)), q[1], s);
+  s = __dp4a(static_cast<int>(prmt(cb, cb, b)), q[2], s);
+  s = __dp4a(static_cast<int>(prmt(cb, cb, b >> 16)), q[3], s);
+  a = w1 & 0x33333333u;
+  b = (w1 >> 2) & 0x33333333u;
+  s = __dp4a(static_cast<int>(prmt(cb, cb, a)), q[4], s);
+  s = __dp4a(static_cast<int>(prmt(cb, cb, a >> 16)), q[5], s);
+  s = __dp4a(static_cast<int>(prmt(cb, cb, b)), q[6], s);
+  s = __dp4a(static_cast<int>(prmt(cb, cb, b >> 16)), q[7], s);
+  return s;
+}
+
+// FP3 selectors for the four (w, h) groups of 8 elements: low two bits from
+// w0/w1, bit 2 moved from w2 to nibble bit 2 by one shift.
+struct Fp3Sel {
+  uint32_t s00, s01, s10, s11;
+};
+
+__device__ __forceinline__ Fp3Sel fp3_selectors(uint32_t w0, uint32_t w1, uint32_t w2) {
+  Fp3Sel s;
+  s.s00 = (w0 & 0x33333333u) | (w2 & 0x44444444u);
+  s.s01 = ((w0 >> 2) & 0x33333333u) | ((w2 >> 1) & 0x44444444u);
+  s.s10 = (w1 & 0x33333333u) | ((w2 << 2) & 0x44444444u);
+  s.s11 = ((w1 >> 2) & 0x33333333u) | ((w2 << 1) & 0x44444444u);
+  return s;
+}
+
+// FP3: cb0 = entries 0..3, cb1 = entries 4..7.
+__device__ __forceinline__ int dot_fp3(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cb0,
+                                       uint32_t cb1, const int* q) {
+  Fp3Sel t = fp3_selectors(w0, w1, w2);
+  int s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s00)), q[0], 0);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s00 >> 16)), q[1], s);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s01)), q[2], s);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s01 >> 16)), q[3], s);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s10)), q[4], s);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s10 >> 16)), q[5], s);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s11)), q[6], s);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s11 >> 16)), q[7], s);
+  return s;
+}
+
+// FP4 expansion of one word (8 codes in nibbles) into two words of int8 values.
+// Entries 0..7 and 8..15 are looked up with 3-bit selectors; bit 3 of each code
+// becomes a 0x00/0xff byte mask by a sign-replicating permute (selector nibble
+// 8 | byte) and blends the two lookups.
+__device__ __forceinline__ void fp4_expand(uint32_t w, uint32_t c0, uint32_t c1, uint32_t c2,
+                                           uint32_t c3, uint32_t& v0, uint32_t& v1) {
+  const uint32_t s = w & 0x77777777u;
+  const uint32_t t = w << 4;
+  const uint32_t lo0 = prmt(c0, c1, s), hi0 = prmt(c2, c3, s);
+  const uint32_t m0 = prmt(t, w, 0xD9C8u);  // bit 3 of codes 0..3
+  const uint32_t s1 = s >> 16;
+  const uint32_t lo1 = prmt(c0, c1, s1), hi1 = prmt(c2, c3, s1);
+  const uint32_t m1 = prmt(t, w, 0xFBEAu);  // bit 3 of codes 4..7
+  v0 = (hi0 & m0) | (lo0 & ~m0);
+  v1 = (hi1 & m1) | (lo1 & ~m1);
+}
+
+__device__ __forceinline__ int dot_fp4(uint4 wd, const uint32_t* cb, const int* q) {
+  uint32_t v0, v1;
+  fp4_expand(wd.x, cb[0], cb[1], cb[2], cb[3], v0, v1);
+  int s = __dp4a(static_cast<int>(v0), q[0], 0);
+  s = __dp4a(static_cast<int>(v1), q[1], s);
+  fp4_expand(wd.y, cb[0], cb[1], cb[2], cb[3], v0, v1);
+  s = __dp4a(static_cast<int>(v0), q[2], s);
+  s = __dp4a(static_cast<int>(v1), q[3], s);
+  fp4_expand(wd.z, cb[0], cb[1], cb[2], cb[3], v0, v1);
+  s = __dp4a(static_cast<int>(v0), q[4], s);
+  s = __dp4a(static_cast<int>(v1), q[5], s);
+  fp4_expand(wd.w, cb[0], cb[1], cb[2], cb[3], v0, v1);
+  s = __dp4a(static_cast<int>(v0), q[6], s);
+  s = __dp4a(static_cast<int>(v1), q[7], s);
+  return s;
+}
+
+// Generic: block (codes at p, shared or global memory) dotted with q, for the
+// compile-time format FMT. cb holds (1 << FMT) / 4 codebook words.
+template <int FMT>
+__device__ __forceinline__ int block_dot(const uint8_t* p, const uint32_t* cb, const int* q) {
+  if constexpr (FMT == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    return dot_fp2(w.x, w.y, cb[0], q);
+  } else if constexpr (FMT == 3) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+    return dot_fp3(w[0], w[1], w[2], cb[0], cb[1], q);
+  } else {
+    return dot_fp4(*reinterpret_cast<const uint4*>(p), cb, q);
+  }
+}
+
+template <int FMT>
+__host__ __device__ constexpr int block_bytes() {
+  return FMT == 2 ? 8 : FMT == 3 ? 12 : 16;
+}
+
+template <int FMT>
+__device__ __forceinline__ float block_scale(const uint8_t* scales, int i) {
+  if constexpr (FMT == 4) {
+    return e8m0_to_f32(scales[i]);
+  } else {
+    return f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scales)[i]);
+  }
+}
+
+// ------------------------------------------------------------------ Q8 and H32
+// Q8 of one 32-block held by one thread (v[32] fp32): amax, d = fp16(amax/127)
+// (IEEE division), r = 1/d (IEEE), q = clamp(rint(v*r), -127, 127).
+__device__ __forceinline__ uint16_t q8_thread(const float* v, int* qw) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+  const float df = __half2float(dh);
+  if (df == 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qw[i] = 0;
+  } else {
+    const float r = __frcp_rn(df);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        int qi = __float2int_rn(__fmul_rn(v[4 * i + t], r));
+        qi = max(-127, min(127, qi));
+        w |= (static_cast<uint32_t>(qi) & 0xffu) << (8 * t);
+      }
+      qw[i] = static_cast<int>(w);
+    }
+  }
+  return __half_as_ushort(dh);
+}
+
+// Q8 of one 32-block spread over a warp (lane i holds element i).
+__device__ __forceinline__ int8_t q8_warp(float v, uint16_t& dbits) {
+  float amax = fabsf(v);
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+  dbits = __half_as_ushort(dh);
+  const float df = __half2float(dh);
+  if (df == 0.0f) return 0;
+  int qi = __float2int_rn(__fmul_rn(v, __frcp_rn(df)));
+  return static_cast<int8_t>(max(-127, min(127, qi)));
+}
+
+// H32 of one 32-block held by one thread: signs, then butterfly stages 0..4.
+__device__ __forceinline__ void h32_thread(float* v, uint32_t signs) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if ((signs >> i) & 1u) v[i] = -v[i];
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int bit = 1 << st;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i & bit) continue;
+      const float a = v[i], b = v[i | bit];
+      v[i] = __fadd_rn(a, b);
+      v[i | bit] = __fsub_rn(a, b);
+    }
+  }
+}
+
+// H32 of one 32-block spread over a warp (lane i holds element i).
+__device__ __forceinline__ float h32_warp(float v, uint32_t signs, int lane) {
+  if ((signs >> lane) & 1u) v = -v;
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int bit = 1 << st;
+    const float o = __shfl_xor_sync(0xffffffffu, v, bit);
+    v = (lane & bit) ? __fsub_rn(o, v) : __fadd_rn(v, o);
+  }
+  return v;
+}
+
+// Canonical router-order warp sum: combining rounds 16, 8, 4, 2, 1.
+__device__ __forceinline__ float warp_sum_canonical(float a) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, d));
+  return a;
+}
+
+// Top-k selection ordering: larger value first, lower index on ties, NaN last.
+__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
+  const bool na = isnan(a), nb = isnan(b);
+  if (na != nb) return nb;
+  if (!na && a != b) return a > b;
+  return ia < ib;
+}
+
+}  // namespace moeq

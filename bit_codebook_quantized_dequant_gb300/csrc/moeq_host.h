@@ -1,0 +1,60 @@
+// Host-side internals of the moeq library: the device view of a packed matrix,
+// descriptor validation and cached device attributes.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moeq.h"
+
+namespace moeq {
+
+// Device view of one role's matrices (plain data, passed to kernels by value).
+struct DMat {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const int8_t* cb;
+  unsigned long long stride_codes;   // bytes between experts
+  unsigned long long stride_scales;  // bytes between experts
+  int cb_stride;                     // bytes between codebook records
+  int rows, cols, fmt;
+};
+
+inline int fmt_block_bytes(int fmt) { return fmt == 2 ? 8 : fmt == 3 ? 12 : fmt == 4 ? 16 : 0; }
+inline int fmt_scale_bytes(int fmt) { return fmt == 4 ? 1 : 2; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline DMat to_dmat(const moeq_matrix& m) {
+  DMat d;
+  d.codes = static_cast<const uint8_t*>(m.codes);
+  d.scales = static_cast<const uint8_t*>(m.scales);
+  d.cb = m.codebooks;
+  d.stride_codes = m.expert_stride_codes;
+  d.stride_scales = m.expert_stride_scales;
+  d.cb_stride = m.cb_stride;
+  d.rows = m.rows;
+  d.cols = m.cols;
+  d.fmt = m.fmt;
+  return d;
+}
+
+// Checks one matrix descriptor against an expected shape. Returns MOEQ_OK or
+// an error code; codebook checks follow the order missing, truncated,
+// mismatched, duplicated.
+int validate_matrix(const moeq_matrix& m, int rows, int cols, int experts);
+
+// Checks a layer descriptor (all roles, shapes, router, signs).
+int validate_layer(const moeq_layer* L);
+
+// Cached per-device attributes.
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  size_t max_smem_optin;
+};
+const DeviceInfo& device_info();
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOEQ_ERR_CUDA; }
+
+}  // namespace moeq

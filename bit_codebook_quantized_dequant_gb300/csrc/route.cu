@@ -1,0 +1,241 @@
+// Router + top-k for T tokens, the H32 rotation and the RMSNorm of the layer
+// stack.
+//
+// Router ("DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
+// 395", section "Decode: up to 32 tok/s": routing with dedicated TOP_K
+// kernels): a CTA takes 8 tokens; their bf16 rows sit in shared memory and each
+// warp streams router rows from global memory (16-byte loads, lane j reading
+// elements 256 i + 8 j .. +7), accumulating the 8 tokens' dot products in fp32
+// in that order, then the combining rounds 16, 8, 4, 2, 1. The logits stay in
+// shared memory and one warp per token selects the top k.
+#include <cuda_runtime.h>
+
+#include "moeq.h"
+#include "moeq_device.cuh"
+#include "moeq_host.h"
+#include "moeq_layout.h"
+
+namespace moeq {
+namespace {
+
+constexpr int kRtTokens = 8;
+constexpr int kRtWarps = 16;
+constexpr int kRtMaxEPerLane = 32;  // E <= 1024
+
+// Top-k + softmax weights of one token by one warp from E logits in memory `l`.
+__device__ void warp_topk(const float* l, int E, int k, int lane, int32_t* idx_out,
+                          float* w_out) {
+  const int nper = (E + 31) / 32;
+  float v[kRtMaxEPerLane];
+  uint32_t valid = 0;
+#pragma unroll
+  for (int i = 0; i < kRtMaxEPerLane; ++i) {
+    const bool ok = i < nper && lane + 32 * i < E;
+    v[i] = ok ? l[lane + 32 * i] : 0.0f;
+    valid |= (ok ? 1u : 0u) << i;
+  }
+  uint32_t taken = 0;
+  int sel[kMaxK];
+  float selv[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    sel[s] = 0;
+    selv[s] = 0.0f;
+    if (s >= k) continue;
+    float bv = 0.0f;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < kRtMaxEPerLane; ++i) {
+      if (!((valid >> i) & 1u) || ((taken >> i) & 1u)) continue;
+      const int e = lane + 32 * i;
+      if (bi < 0 || ranks_before(v[i], e, bv, bi)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    sel[s] = bi;
+    selv[s] = bv;
+  }
+  const float m = selv[0];
+  float z = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kRtMaxEPerLane; ++i)
+    if (((valid >> i) & 1u) && !isnan(v[i])) z += expf(v[i] - m);
+  z = warp_sum_canonical(z);
+  if (lane < k) {
+    int my = 0;
+    float mv = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s)
+      if (s == lane) {
+        my = sel[s];
+        mv = selv[s];
+      }
+    idx_out[lane] = my;
+    w_out[lane] = __fdiv_rn(expf(mv - m), z);
+  }
+}
+
+__global__ void __launch_bounds__(kRtWarps * 32) route_kernel(
+    const uint16_t* __restrict__ x, int T, const uint16_t* __restrict__ router, int E, int H,
+    int k, int32_t* __restrict__ idx, float* __restrict__ w, float* __restrict__ logits_out) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);                           // [8][H]
+  float* ls = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(kRtTokens) * H * 2);  // [8][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * kRtTokens;
+  const int nt = min(kRtTokens, T - t0);
+  const int vec_per_row = H / 8;
+  for (int i = tid; i < kRtTokens * vec_per_row; i += blockDim.x) {
+    const int tt = i / vec_per_row, c = i % vec_per_row;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tt < nt) v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + tt) * H) + c);
+    reinterpret_cast<uint4*>(xs + static_cast<size_t>(tt) * H)[c] = v;
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += kRtWarps) {
+    const uint16_t* wr = router + static_cast<size_t>(e) * H;
+    float acc[kRtTokens];
+#pragma unroll
+    for (int tt = 0; tt < kRtTokens; ++tt) acc[tt] = 0.0f;
+    for (int i = 0; i < H / 256; ++i) {
+      const int k0 = 256 * i + 8 * lane;
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wr + k0));
+#pragma unroll
+      for (int tt = 0; tt < kRtTokens; ++tt) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + static_cast<size_t>(tt) * H + k0);
+        float a = acc[tt];
+        a = fmaf(bf16_lo(xv.x), bf16_lo(wv.x), a);
+        a = fmaf(bf16_hi(xv.x), bf16_hi(wv.x), a);
+        a = fmaf(bf16_lo(xv.y), bf16_lo(wv.y), a);
+        a = fmaf(bf16_hi(xv.y), bf16_hi(wv.y), a);
+        a = fmaf(bf16_lo(xv.z), bf16_lo(wv.z), a);
+        a = fmaf(bf16_hi(xv.z), bf16_hi(wv.z), a);
+        a = fmaf(bf16_lo(xv.w), bf16_lo(wv.w), a);
+        a = fmaf(bf16_hi(xv.w), bf16_hi(wv.w), a);
+        acc[tt] = a;
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < kRtTokens; ++tt) {
+      const float l = warp_sum_canonical(acc[tt]);
+      if (lane == 0) {
+        ls[tt * E + e] = l;
+        if (logits_out && tt < nt) logits_out[static_cast<size_t>(t0 + tt) * E + e] = l;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < nt)
+    warp_topk(ls + warp * E, E, k, lane, idx + static_cast<size_t>(t0 + warp) * k,
+              w + static_cast<size_t>(t0 + warp) * k);
+}
+
+__global__ void h32_kernel(const float* __restrict__ in, float* out, int nblk,
+                           const uint32_t* __restrict__ signs) {
+  const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= nblk) return;
+  const float v = in[static_cast<size_t>(b) * 32 + lane];
+  out[static_cast<size_t>(b) * 32 + lane] = h32_warp(v, signs ? signs[b] : 0u, lane);
+}
+
+// One warp per row: sum of squares in the canonical order, correctly rounded
+// fp32 steps, then a = bf16_rne(r * inv).
+__global__ void rmsnorm_kernel(const float* __restrict__ r, int T, int H, uint16_t* __restrict__ a) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = r + static_cast<size_t>(t) * H;
+  float s = 0.0f;
+  for (int i = 0; i < H / 256; ++i) {
+    const float4 v0 = *reinterpret_cast<const float4*>(row + 256 * i + 8 * lane);
+    const float4 v1 = *reinterpret_cast<const float4*>(row + 256 * i + 8 * lane + 4);
+    s = __fadd_rn(s, __fmul_rn(v0.x, v0.x));
+    s = __fadd_rn(s, __fmul_rn(v0.y, v0.y));
+    s = __fadd_rn(s, __fmul_rn(v0.z, v0.z));
+    s = __fadd_rn(s, __fmul_rn(v0.w, v0.w));
+    s = __fadd_rn(s, __fmul_rn(v1.x, v1.x));
+    s = __fadd_rn(s, __fmul_rn(v1.y, v1.y));
+    s = __fadd_rn(s, __fmul_rn(v1.z, v1.z));
+    s = __fadd_rn(s, __fmul_rn(v1.w, v1.w));
+  }
+  s = warp_sum_canonical(s);
+  const float ms = __fdiv_rn(s, static_cast<float>(H));
+  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, 1e-6f)));
+  uint16_t* out = a + static_cast<size_t>(t) * H;
+  for (int k0 = 8 * lane; k0 < H; k0 += 256) {
+    const float4 v0 = *reinterpret_cast<const float4*>(row + k0);
+    const float4 v1 = *reinterpret_cast<const float4*>(row + k0 + 4);
+    uint4 o;
+    o.x = f32_to_bf16_rne(__fmul_rn(v0.x, inv)) | (static_cast<uint32_t>(f32_to_bf16_rne(__fmul_rn(v0.y, inv))) << 16);
+    o.y = f32_to_bf16_rne(__fmul_rn(v0.z, inv)) | (static_cast<uint32_t>(f32_to_bf16_rne(__fmul_rn(v0.w, inv))) << 16);
+    o.z = f32_to_bf16_rne(__fmul_rn(v1.x, inv)) | (static_cast<uint32_t>(f32_to_bf16_rne(__fmul_rn(v1.y, inv))) << 16);
+    o.w = f32_to_bf16_rne(__fmul_rn(v1.z, inv)) | (static_cast<uint32_t>(f32_to_bf16_rne(__fmul_rn(v1.w, inv))) << 16);
+    *reinterpret_cast<uint4*>(out + k0) = o;
+  }
+}
+
+}  // namespace
+
+// Enqueues router + top-k (used by moe_route_topk and by the prefill).
+int route_topk_launch(const uint16_t* x, int T, const uint16_t* router, int E, int H, int k,
+                      int32_t* idx, float* w, float* logits, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(kRtTokens) * H * 2 + static_cast<size_t>(kRtTokens) * E * 4;
+  const DeviceInfo& di = device_info();
+  if (smem > di.max_smem_optin) return MOEQ_ERR_SHAPE;
+  if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOEQ_ERR_CUDA;
+  const int grid = (T + kRtTokens - 1) / kRtTokens;
+  route_kernel<<<grid, kRtWarps * 32, smem, s>>>(x, T, router, E, H, k, idx, w, logits);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moeq
+
+using namespace moeq;
+
+extern "C" int moe_route_topk(const uint16_t* x, int T, const uint16_t* router, int E, int H, int k,
+                              int32_t* idx, float* w, float* logits_opt, int32_t* dev_status,
+                              moeq_stream stream) {
+  (void)dev_status;
+  if (T < 0 || E < 1 || E > 1024 || H < 256 || H % 256) return MOEQ_ERR_SHAPE;
+  if (k < 1 || k > kMaxTopK || k > E) return MOEQ_ERR_ARG;
+  if (T == 0) return MOEQ_OK;
+  if (!x || !router || !idx || !w) return MOEQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(router)) return MOEQ_ERR_ALIGN;
+  return route_topk_launch(x, T, router, E, H, k, idx, w, logits_opt,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int h32_rotate(const float* in, float* out, int nblk, const uint32_t* signs,
+                          moeq_stream stream) {
+  if (nblk < 0) return MOEQ_ERR_SHAPE;
+  if (nblk == 0) return MOEQ_OK;
+  if (!in || !out) return MOEQ_ERR_ARG;
+  const int per = 8;  // blocks per CTA
+  h32_kernel<<<(nblk + per - 1) / per, per * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      in, out, nblk, signs);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" int moe_rmsnorm_bf16(const float* r, int T, int H, uint16_t* a, moeq_stream stream) {
+  if (T < 0 || H < 256 || H % 256) return MOEQ_ERR_SHAPE;
+  if (T == 0) return MOEQ_OK;
+  if (!r || !a) return MOEQ_ERR_ARG;
+  if (!aligned16(r) || !aligned16(a)) return MOEQ_ERR_ALIGN;
+  const int per = 8;
+  rmsnorm_kernel<<<(T + per - 1) / per, per * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(r, T, H, a);
+  return cuda_status(cudaGetLastError());
+}

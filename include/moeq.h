@@ -1,0 +1,201 @@
+/*
+ * moeq -- codebook-quantized mixture-of-experts FFN for GB300 (sm_103a).
+ *
+ * C ABI. Plain pointers and sizes; no framework types. Unless stated
+ * otherwise every pointer argument is a DEVICE pointer owned by the caller,
+ * every call only enqueues work on the given CUDA stream (no call
+ * synchronizes with the host), and the library allocates no device memory.
+ *
+ * Errors in arguments, shapes, alignment, formats and codebooks are returned
+ * synchronously as a negative moeq_status before anything is enqueued.
+ * Errors found on the device (a bounded wait that ran out, an index out of
+ * range) are written as a nonzero value into *dev_status, a device int32 the
+ * caller zeroes and reads after its own synchronization. No kernel traps.
+ *
+ * Formats ("DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
+ * 395", section "ROCmFPX: fitting 284B weights into 128 GB"): 32-weight blocks
+ * of packed low-bit codes plus a small scale -- FP2 10 B/block (2.50 bpw),
+ * FP3 14 B/block (3.50 bpw), FP4 17 B/block (4.25 bpw) -- with a per-expert
+ * int8 codebook ("Lucebox x Geometric: DeepSeek V4 Flash 0731 reaches 32.7
+ * tok/s on AMD Strix Halo", section "How the model fits on AMD Strix Halo").
+ * The pages fix sizes, not bits; the layout below is this library's:
+ *
+ *   matrix [rows x cols], cols % 128 == 0, nb = cols / 32 blocks per row
+ *   code plane : block (r, b) at byte (r*nb + b) * Bc, Bc = 8 / 12 / 16
+ *   scale plane: entry r*nb + b, fp16 bits (FP2, FP3) or E8M0 byte (FP4,
+ *                value 2^(e-127), e = 255 invalid)
+ *   FP2 block  : LE words w0, w1; element j = 16w + 8h + n has its code at
+ *                bits 4n+2h .. 4n+2h+1 of word w
+ *   FP3 block  : low two bits as FP2 in w0, w1; bit 2 of element (w, h, n) at
+ *                bit 4n + p(w,h) of w2, p(0,0)=2, p(0,1)=3, p(1,0)=0, p(1,1)=1
+ *   FP4 block  : element j in nibble j%8 of word j/8
+ *   weight     : scale(r, b) * codebook[code]
+ */
+#ifndef MOEQ_H
+#define MOEQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moeq_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum { MOEQ_FP2 = 2, MOEQ_FP3 = 3, MOEQ_FP4 = 4 } moeq_fmt;
+
+typedef enum {
+  MOEQ_OK = 0,
+  MOEQ_ERR_ARG = -1,                 /* NULL where a pointer is required, bad k, T, ... */
+  MOEQ_ERR_SHAPE = -2,               /* unsupported or inconsistent sizes */
+  MOEQ_ERR_ALIGN = -3,               /* pointer or stride not 16-byte aligned */
+  MOEQ_ERR_FORMAT = -4,              /* fmt not 2, 3 or 4, or not allowed for the role */
+  MOEQ_ERR_CODEBOOK_MISSING = -5,    /* codebooks == NULL */
+  MOEQ_ERR_CODEBOOK_TRUNCATED = -6,  /* cb_len < 2^fmt */
+  MOEQ_ERR_CODEBOOK_MISMATCH = -7,   /* cb_len > 2^fmt */
+  MOEQ_ERR_CODEBOOK_DUPLICATE = -8,  /* per-expert codebook records overlap (stride < len) */
+  MOEQ_ERR_WORKSPACE = -9,           /* workspace NULL, too small or misaligned */
+  MOEQ_ERR_CUDA = -10,               /* a CUDA runtime call failed */
+  MOEQ_ERR_DEVICE_TIMEOUT = -11,     /* (device status) a bounded wait ran out */
+  MOEQ_ERR_DEVICE_INDEX = -12        /* (device status) an index read on the device was out of range */
+} moeq_status;
+
+/* All experts of one role (e.g. the 256 routed gate matrices) share format and
+ * shape; expert e's planes start at codes + e*expert_stride_codes and
+ * scales + e*expert_stride_scales; its codebook at codebooks + e*cb_stride. */
+typedef struct {
+  int fmt;                      /* moeq_fmt */
+  int rows, cols;               /* cols % 128 == 0 */
+  int num_experts;              /* E for routed roles, 1 for shared / dense */
+  const void* codes;            /* 16-byte aligned */
+  size_t expert_stride_codes;   /* bytes, multiple of 16 */
+  const void* scales;           /* 16-byte aligned */
+  size_t expert_stride_scales;  /* bytes, multiple of 16 */
+  const int8_t* codebooks;      /* [num_experts] records of cb_len int8 */
+  int cb_len;                   /* must equal 2^fmt */
+  int cb_stride;                /* bytes between records, >= cb_len */
+} moeq_matrix;
+
+typedef struct {
+  int H, I, E, k;               /* hidden, expert intermediate, experts, top-k */
+  const uint16_t* router;       /* bf16 [E x H] row-major */
+  moeq_matrix gate, up;         /* [I x H] per expert */
+  moeq_matrix down;             /* [H x I] per expert */
+  int has_shared;               /* 1: always-on shared expert with weight 1 */
+  moeq_matrix sgate, sup, sdown;
+  const uint32_t* h32_signs_x;  /* [H/32] H32 sign masks for x, NULL = no rotation */
+  const uint32_t* h32_signs_h;  /* [I/32] H32 sign masks for h, NULL = no rotation */
+} moeq_layer;
+
+/* Optional intermediates for parity tests; any pointer may be NULL. For
+ * T tokens, "slots" = k routed experts followed by the shared one (if any). */
+typedef struct {
+  int8_t* xq; uint16_t* xd;     /* [T x H], [T x H/32] quantized (rotated) input */
+  float* logits;                /* [T x E] */
+  int32_t* idx; float* p;       /* [T x k] expert indices, combine weights */
+  float* h;                     /* [T x slots x I] SwiGLU output before rotation */
+  int8_t* hq; uint16_t* hd;     /* [T x slots x I], [T x slots x I/32] */
+  float* o;                     /* [T x slots x H] expert outputs before the combine */
+  int32_t* S_gate, *S_up;       /* decode only: [slots x I x H/32] int32 block partials */
+  int32_t* S_down;              /* decode only: [slots x H x I/32] */
+} moeq_debug;
+
+/* ---------------------------------------------------------------- sizes */
+
+/* Bytes of the two planes of one packed matrix. Returns MOEQ_OK or an error. */
+int moeq_packed_bytes(int fmt, int rows, int cols, size_t* code_bytes, size_t* scale_bytes);
+
+/* Host-side checks of a layer descriptor (shapes, formats, alignment,
+ * codebook records); enqueues nothing. The codebook checks mirror the loader
+ * validation for "missing, duplicated, truncated, or mismatched codebooks" of
+ * "Lucebox x Geometric ...", section "Lucebox Engine integration with
+ * Geometric". Returns MOEQ_OK or the first error found. */
+int moeq_validate_layer(const moeq_layer* L);
+
+/* Workspace bytes for a call: mode 0 = decode, 1 = q=4 verify, 2 = prefill of
+ * up to T_max tokens. 0 on an invalid descriptor. */
+size_t moe_ffn_workspace(const moeq_layer* L, int T_max, int mode);
+
+/* Zero a freshly allocated workspace (enqueued memset). Needed once; every
+ * FFN call leaves the workspace ready for the next one on the same stream. */
+int moe_ffn_workspace_init(void* ws, size_t ws_bytes, moeq_stream stream);
+
+/* ---------------------------------------------------------------- entry points */
+
+/* Pack one matrix: codes_u8 [rows x cols] (one code per byte, < 2^fmt) and
+ * scales [rows x cols/32] (fp16 bits or E8M0 bytes, row-major) into the code
+ * plane out_codes and the scale plane out_scales (the scale plane has the
+ * input's layout; it is copied). A code out of range sets *dev_status to
+ * MOEQ_ERR_DEVICE_INDEX and is packed masked to fmt bits. */
+int moe_pack_expert(int fmt, int rows, int cols, const uint8_t* codes_u8, const void* scales,
+                    void* out_codes, void* out_scales, int32_t* dev_status, moeq_stream stream);
+
+/* Router and top-k for T tokens ("DeepSeek V4 Flash: 284B model ...", section
+ * "Decode: up to 32 tok/s": routing with dedicated TOP_K kernels):
+ * logits[t,e] = sum_h router[e,h] x[t,h] with bf16 operands and an fp32 sum in
+ * the canonical order (32 partials j over h = 256 i + 8 j + t', then pairwise
+ * rounds 16, 8, 4, 2, 1); idx = the k largest (ties to the lower index);
+ * w = softmax over all E logits at those indices (no renormalization).
+ * x [T x H] bf16, router [E x H] bf16, idx [T x k], w [T x k], logits_opt
+ * [T x E] or NULL. H % 256 == 0, 1 <= k <= min(E, 8), E <= 1024. */
+int moe_route_topk(const uint16_t* x, int T, const uint16_t* router, int E, int H, int k,
+                   int32_t* idx, float* w, float* logits_opt, int32_t* dev_status,
+                   moeq_stream stream);
+
+/* Batch-1 decode of one layer: y [H] fp32 from x [H] bf16 (see the layer
+ * comment above for the computation: Q8 of the optionally H32-rotated x,
+ * router + top-k, per selected expert fused dequant gate/up GEMV, SwiGLU,
+ * optional H32 + Q8 of h, down GEMV, combine sum_slot p*o + shared in slot
+ * order). One persistent cooperative kernel; no host synchronization
+ * ("Lucebox x Geometric ...", section "Lucebox Engine integration with
+ * Geometric": fused matvec and sync-free MoE decode). ws: a workspace of
+ * moe_ffn_workspace(L, 1, 0) bytes, zeroed once with moe_ffn_workspace_init;
+ * calls that share a workspace must be ordered (same stream). dbg may be NULL.
+ * Requires H, I <= 4096 and multiples of 256; k <= 8. */
+int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, void* ws, size_t ws_bytes,
+                   int32_t* dev_status, const moeq_debug* dbg, moeq_stream stream);
+
+/* q=4 verification ("DeepSeek V4 Flash: 284B model ...", section "Decode: up
+ * to 32 tok/s"): four columns x [4 x H], each routed independently,
+ * y [4 x H] = the decode of each column; every packed block of every expert,
+ * of the shared expert and of the optional dense FP4 [H x H] projection is
+ * expanded once per call and applied to every column that uses it;
+ * y_dense [4 x H] = dense * Q8(column) (NULL dense -> y_dense untouched).
+ * ws: moe_ffn_workspace(L, 4, 1) bytes. */
+int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, const uint16_t* x, float* y,
+                      float* y_dense, void* ws, size_t ws_bytes, int32_t* dev_status,
+                      const moeq_debug* dbg, moeq_stream stream);
+
+/* Expert-grouped prefill of T tokens ("deepseek-v4-flash-0731-evox3-rocm",
+ * section "The optimization ladder": fused multi-token prefill): per token
+ * the same result as moe_ffn_decode, computed as router + top-k for all
+ * tokens, a stable counting sort of (token, slot) pairs by expert, grouped
+ * GEMMs for gate/up (+SwiGLU, H32, Q8 of h) and down, and a gather-combine in
+ * slot order. If residual is not NULL, y = residual + FFN(x) (the residual
+ * add of a stacked layer; y may equal residual). x [T x H] bf16, y [T x H]
+ * fp32. ws: moe_ffn_workspace(L, T, 2) bytes. */
+int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, const float* residual, float* y,
+                    void* ws, size_t ws_bytes, int32_t* dev_status, const moeq_debug* dbg,
+                    moeq_stream stream);
+
+/* H32 rotation ("deepseek-v4-flash-0731-evox3-rocm", section "The optimization
+ * ladder"): out = H D in per 32-block, H the 32x32 Sylvester Hadamard matrix
+ * (unnormalized), D = diag(-1 where bit i of signs[b] is set); fp32 butterfly
+ * stages 0..4, (a, b) -> (a + b, a - b). signs NULL = no sign flips. in and
+ * out [nblk x 32] fp32 (may alias). */
+int h32_rotate(const float* in, float* out, int nblk, const uint32_t* signs, moeq_stream stream);
+
+/* RMSNorm with unit weight between stacked layers, rounded to bf16:
+ * a[t,:] = bf16_rne(r[t,:] / sqrt(sum(r^2)/H + 1e-6)) with the sum of squares
+ * in fp32 in the router's canonical order and correctly rounded fp32
+ * operations. r [T x H] fp32, a [T x H] bf16, H % 256 == 0. */
+int moe_rmsnorm_bf16(const float* r, int T, int H, uint16_t* a, moeq_stream stream);
+
+/* Version string of the library build. */
+const char* moeq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+descriptor validation returns the documented codes (no GPU work)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import bit_codebook_quantized_dequant_gb300 as M
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in ("moeq.h", "moeq_synth.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = M.load()
+    names = _declared()
+    assert {"moe_pack_expert", "moe_route_topk", "moe_ffn_decode", "moe_ffn_verify_q4",
+            "moe_ffn_prefill", "h32_rotate"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(M.EXPORTED) == names
+    assert M.moeq_version().startswith("moeq")
+
+
+def test_packed_bytes():
+    assert M.moeq_packed_bytes(2, 2048, 4096) == (2048 * 128 * 8, 2048 * 128 * 2)
+    assert M.moeq_packed_bytes(3, 4096, 2048) == (4096 * 64 * 12, 4096 * 64 * 2)
+    assert M.moeq_packed_bytes(4, 2048, 4096) == (2048 * 128 * 16, 2048 * 128)
+    with pytest.raises(M.MoeqError):
+        M.moeq_packed_bytes(5, 1, 32)
+
+
+FAKE = 1 << 40  # aligned fake device address: validation never dereferences
+
+
+def _mat(fmt, rows, cols, E, **kw):
+    cb, sb = M.moeq_packed_bytes(fmt, rows, cols)
+    d = dict(fmt=fmt, rows=rows, cols=cols, num_experts=E, codes=FAKE, expert_stride_codes=cb,
+             scales=FAKE, expert_stride_scales=(sb + 15) // 16 * 16, codebooks=FAKE,
+             cb_len=1 << fmt, cb_stride=1 << fmt)
+    d.update(kw)
+    return M.MoeqMatrix(**d)
+
+
+def _layer(**over):
+    L = M.MoeqLayer()
+    L.H, L.I, L.E, L.k = 256, 256, 16, 2
+    L.router = FAKE
+    L.gate = _mat(2, 256, 256, 16)
+    L.up = _mat(2, 256, 256, 16)
+    L.down = _mat(3, 256, 256, 16)
+    for k, v in over.items():
+        setattr(L, k, v)
+    return L
+
+
+def test_validation_codes():
+    assert M.moeq_validate_layer(_layer()) == 0
+    assert M.moe_ffn_workspace(_layer(), 1, 0) > 0
+    cases = {
+        "MOEQ_ERR_CODEBOOK_MISSING": dict(gate=_mat(2, 256, 256, 16, codebooks=None)),
+        "MOEQ_ERR_CODEBOOK_TRUNCATED": dict(down=_mat(3, 256, 256, 16, cb_len=4)),
+        "MOEQ_ERR_CODEBOOK_MISMATCH": dict(up=_mat(2, 256, 256, 16, cb_len=8, cb_stride=8)),
+        "MOEQ_ERR_CODEBOOK_DUPLICATE": dict(gate=_mat(2, 256, 256, 16, cb_stride=0)),
+        "MOEQ_ERR_FORMAT": dict(gate=M.MoeqMatrix(5, 256, 256, 16, FAKE, 1 << 20, FAKE, 1 << 20,
+                                                  FAKE, 32, 32)),
+        "MOEQ_ERR_SHAPE": dict(H=200),
+        "MOEQ_ERR_ALIGN": dict(router=FAKE + 8),
+        "MOEQ_ERR_ARG": dict(k=0),
+    }
+    for code, over in cases.items():
+        assert M.moeq_validate_layer(_layer(**over)) == M.CODE[code], code
+    assert M.moeq_validate_layer(_layer(k=17)) == M.CODE["MOEQ_ERR_ARG"]
+    assert M.moe_ffn_workspace(_layer(H=200), 1, 0) == 0
+    # a gate/up format mismatch is a format error
+    assert M.moeq_validate_layer(_layer(up=_mat(4, 256, 256, 16))) == M.CODE["MOEQ_ERR_FORMAT"]
+
+
+def test_entry_points_reject_bad_arguments_before_launch():
+    lib = M.load()
+    L = _layer()
+    # NULL x / y and a NULL workspace are rejected synchronously, nothing enqueued
+    assert lib.moe_ffn_decode(C.byref(L), None, None, None, 0, None, None, None) == \
+        M.CODE["MOEQ_ERR_ARG"]
+    assert lib.moe_ffn_decode(C.byref(L), FAKE, FAKE, None, 0, None, None, None) == \
+        M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert lib.moe_pack_expert(7, 1, 32, FAKE, FAKE, FAKE, FAKE, None, None) == \
+        M.CODE["MOEQ_ERR_FORMAT"]
+    assert lib.moe_pack_expert(2, 1, 32, FAKE + 4, FAKE, FAKE, FAKE, None, None) == \
+        M.CODE["MOEQ_ERR_ALIGN"]
+    assert lib.moe_route_topk(FAKE, 1, FAKE, 16, 100, 2, FAKE, FAKE, None, None, None) == \
+        M.CODE["MOEQ_ERR_SHAPE"]
+    assert lib.moe_route_topk(FAKE, 1, FAKE, 16, 256, 9, FAKE, FAKE, None, None, None) == \
+        M.CODE["MOEQ_ERR_ARG"]
+    assert lib.h32_rotate(None, None, 4, None, None) == M.CODE["MOEQ_ERR_ARG"]
+    assert lib.moe_rmsnorm_bf16(FAKE, 1, 100, FAKE, None) == M.CODE["MOEQ_ERR_SHAPE"]

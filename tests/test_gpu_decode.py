@@ -1,0 +1,130 @@
+"""GPU parity of moe_ffn_decode against the oracle, stage by stage:
+bit-exact xq/xd, logits, indices and int32 block partials (down partials with
+the oracle fed the GPU's quantized h); h within fp32 tolerance; hq/hd equal to
+the oracle's quantizer applied to the GPU's h; y within the output tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import bit_codebook_quantized_dequant_gb300 as M
+from bit_codebook_quantized_dequant_gb300 import synth as S
+from bit_codebook_quantized_dequant_gb300.workload import (Debug, Workspace, build_layer,
+                                                           to_dev_u16)
+from _parity import check_output, host_layer_for, output_bound, slot_bounds
+
+pytestmark = pytest.mark.gpu
+
+
+def _cfg(cfg_id, **over):
+    c = dict(S.CONFIGS[cfg_id])
+    c.update(over)
+    return c
+
+
+def _run(dl, ws, x_row, partials):
+    cfg = dl.cfg
+    dbg = Debug(cfg, 1, partials)
+    y = torch.zeros(cfg["H"], dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_ffn_decode(dl.desc(), to_dev_u16(x_row), y, ws.ptr, ws.nbytes, st, dbg.struct)
+    torch.cuda.synchronize()
+    assert st.item() == 0, M.STATUS.get(st.item())
+    return y.cpu().numpy(), dbg.numpy()
+
+
+def _check_token(L, cfg, x_row, y, g, partials):
+    H, I, k = cfg["H"], cfg["I"], cfg["k"]
+    ns = k + (1 if cfg["shared_fmt"] else 0)
+    yo, tr = O.ffn_decode(L, x_row, trace=True, partials=partials)
+    np.testing.assert_array_equal(g["xq"], tr["xq"])
+    np.testing.assert_array_equal(g["xd"], tr["xd"])
+    np.testing.assert_array_equal(g["logits"], tr["logits"])
+    np.testing.assert_array_equal(g["idx"], tr["idx"])
+    np.testing.assert_allclose(g["p"], tr["p"], rtol=2e-6)
+    h = g["h"].reshape(ns, I)
+    np.testing.assert_allclose(h, tr["h"][:ns], rtol=2e-4, atol=2e-6 * np.abs(tr["h"][:ns]).max())
+    # quantization decision: the oracle's quantizer on the GPU's h, bit for bit
+    hq = g["hq"].reshape(ns, I)
+    hd = g["hd"].reshape(ns, I // 32)
+    for s in range(ns):
+        hh = h[s]
+        if L.signs_h is not None:
+            hh = O.h32_f32(hh, L.signs_h)
+        q, d = O.q8(hh)
+        np.testing.assert_array_equal(hq[s], q)
+        np.testing.assert_array_equal(hd[s], d)
+    # independent quantization differs at most by one step, on rare elements
+    diff = np.abs(hq.astype(int) - tr["hq"][:ns].astype(int))
+    assert diff.max() <= 1 and (diff > 0).sum() <= max(2, 1e-3 * diff.size)
+    # teacher-forced down projection: bit-exact partials, tight y
+    yt, tt = O.ffn_decode(L, x_row, trace=True, partials=partials, force_hq=hq, force_hd=hd)
+    if partials:
+        np.testing.assert_array_equal(g["S_gate"].reshape(ns, I, H // 32), tr["S_gate"][:ns])
+        np.testing.assert_array_equal(g["S_up"].reshape(ns, I, H // 32), tr["S_up"][:ns])
+        np.testing.assert_array_equal(g["S_down"].reshape(ns, H, I // 32), tt["S_down"][:ns])
+    B = output_bound(L, tr["idx"], tr["p"], hq, hd)
+    o = g["o"].reshape(ns, H)
+    for s, bs in enumerate(slot_bounds(L, tr["idx"], hq, hd)):
+        assert np.all(np.abs(o[s] - tt["o"][s]) <= 1e-5 * bs), f"o[{s}]"
+    check_output(y, yt, B, "y (teacher-forced)")
+    same_q = np.array_equal(hq, tr["hq"][:ns]) and np.array_equal(hd, tr["hd"][:ns])
+    return yo, B, same_q
+
+
+@pytest.mark.parametrize("variant", ["cfg0", "cfg0-shared", "cfg0-h32-fp4", "cfg0-fp2-down"])
+def test_decode_tiny(variant):
+    over = {}
+    if variant == "cfg0-shared":
+        over = dict(shared_fmt=4, k=3)
+    elif variant == "cfg0-h32-fp4":
+        over = dict(h32=True, fmt_gu=4, fmt_down=4)
+    elif variant == "cfg0-fp2-down":
+        over = dict(fmt_down=2, shared_fmt=4)
+    cfg = _cfg(0, **over)
+    seed = S.config_seed(0) + 17 * len(variant)
+    dl = build_layer(seed, 0, cfg)
+    ws = Workspace(dl, 0)
+    xs = S.tokens(seed, cfg, 8)
+    L = host_layer_for(seed, 0, cfg, xs)
+    for t in range(xs.shape[0]):
+        y, g = _run(dl, ws, xs[t], partials=True)
+        yo, B, same_q = _check_token(L, cfg, xs[t], y, g, partials=True)
+        if same_q:  # no fp32-vs-fp64 rounding of h crossed a quantization step
+            check_output(y, yo, B, "y (independent)")
+
+
+def test_decode_config1_sampled_tokens():
+    cfg = _cfg(1)
+    seed = S.config_seed(1)
+    dl = build_layer(seed, 0, cfg)
+    ws = Workspace(dl, 0)
+    xs = S.tokens(seed, cfg, 3, start=0)
+    L = host_layer_for(seed, 0, cfg, xs)
+    for t in range(xs.shape[0]):
+        y, g = _run(dl, ws, xs[t], partials=(t == 0))
+        _check_token(L, cfg, xs[t], y, g, partials=(t == 0))
+
+
+def test_decode_repeatable_and_workspace_reused():
+    cfg = _cfg(1)
+    seed = S.config_seed(1)
+    dl = build_layer(seed, 0, cfg)
+    ws = Workspace(dl, 0)
+    xs = S.tokens(seed, cfg, 2, start=100)
+    ys = []
+    for rep in range(3):
+        for t in range(2):
+            y = torch.zeros(cfg["H"], dtype=torch.float32, device="cuda")
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            M.moe_ffn_decode(dl.desc(), to_dev_u16(xs[t]), y, ws.ptr, ws.nbytes, st)
+            torch.cuda.synchronize()
+            assert st.item() == 0
+            ys.append(y.cpu().numpy())
+    for rep in range(1, 3):
+        np.testing.assert_array_equal(ys[2 * rep], ys[0])
+        np.testing.assert_array_equal(ys[2 * rep + 1], ys[1])
+    # counters are back to zero after every call
+    n_ctr = 48 + (cfg["k"] + 1) * (cfg["I"] // 32) + cfg["H"] // 32
+    ctr = ws.buf[: 4 * n_ctr].view(torch.int32).cpu().numpy()
+    assert not ctr.any()
