@@ -50,7 +50,11 @@ class MoeqLayer(C.Structure):
 
 class MoeqDebug(C.Structure):
     _fields_ = [(n, P) for n in ("xq", "xd", "logits", "idx", "p", "h", "hq", "hd", "o", "S_gate",
-                                 "S_up", "S_down")]
+                                 "S_up", "S_down", "trace")] + [("trace_cap", C.c_int)]
+
+
+TRACE_EVENTS = {1: "START", 2: "TAKE", 3: "TOPK", 4: "ISSUED", 5: "READY", 6: "DONE",
+                7: "EPI_BEGIN", 8: "EPI_END", 9: "SPIN"}
 
 
 _lib = None

@@ -35,7 +35,7 @@ int validate_layer(const moeq_layer* L) {
   if (!L) return MOEQ_ERR_ARG;
   const int H = L->H, I = L->I, E = L->E, k = L->k;
   if (H <= 0 || I <= 0 || E <= 0) return MOEQ_ERR_SHAPE;
-  if (H % 256 || I % 256) return MOEQ_ERR_SHAPE;
+  if (H % 256 || I % 128) return MOEQ_ERR_SHAPE;
   if (k < 1 || k > kMaxTopK || k > E) return MOEQ_ERR_ARG;
   if (!L->router) return MOEQ_ERR_ARG;
   if (!aligned16(L->router)) return MOEQ_ERR_ALIGN;

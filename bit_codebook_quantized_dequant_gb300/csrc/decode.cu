@@ -1,27 +1,34 @@
 // Batch-1 decode of one codebook-quantized MoE FFN layer in one persistent,
 // cooperative, warp-specialized kernel.
 //
-// Work is cut into units taken from a global queue in dependency order:
-//   router rows (8 per unit) -> shared-expert gate/up rows (16) -> routed
-//   gate/up rows (16 per unit, slot-major) -> shared down rows (32) -> routed
-//   down rows (32, slot-major).
-// A unit only waits on units with a smaller queue index, and every CTA is
-// resident (cooperative launch), so the waits always end; each is bounded
-// anyway and reports MOEQ_ERR_DEVICE_TIMEOUT into the status word if it runs out.
+// Work items are taken from a global queue in dependency order:
+//   router rows (4 per item)
+//   -> shared-expert gate/up (32 rows per item, as two 16-row fills)
+//   -> routed gate/up (32 rows per item, slot-major)
+//   -> shared down rows (32 per item) -> routed down rows (32, slot-major)
+//   -> (after every down item) the combine of y.
+// An item only waits on items with a smaller queue index, and every CTA is
+// resident (cooperative launch), so every wait ends; each is bounded anyway and
+// reports MOEQ_ERR_DEVICE_TIMEOUT into the status word if it runs out.
 //
-// Per CTA: one producer warp takes units from the queue and streams their
-// packed rows (codes plane and scale plane, contiguous per row range) from HBM
-// into a 3-stage shared-memory ring with bulk asynchronous copies; it also
-// computes the top-k once the router rows are done. Sixteen compute warps
-// expand codes in registers (byte permutes), take int8 dot products per
-// 32-block (dp4a) and apply the block scales in fp32:
-//   * router unit : canonical-order bf16 logits, one warp per row;
-//   * gate/up unit: one warp per row computes g and u, then h = silu(g) u;
-//                   the CTA that finishes the second half of a 32-row block
-//                   rotates (H32) and quantizes (Q8) that block of h;
-//   * down unit   : one warp per two rows computes o; the CTA that writes the
-//                   last slot of a 32-row chunk of y combines the slots in
-//                   order: y = sum_s p_s o_s (+ o_shared).
+// Per CTA (18 warps):
+//   * producer warp: takes items, streams their packed rows (code plane and
+//     scale plane, contiguous per row range) from HBM into a 3-stage shared
+//     memory ring with bulk asynchronous copies; once the routing record is
+//     published it stages the selected experts' codebooks and prefetches their
+//     down rows into L2; for a down item it waits until that slot's quantized h
+//     is complete and copies it into the stage next to the weights;
+//   * two compute groups of 8 warps, on alternate stage fills: expand codes in
+//     registers (byte permutes), take int8 dot products per 32-block (dp4a),
+//     apply the block scales in fp32, release the stage as soon as it is read,
+//     and hand the fill to the epilogue warp;
+//   * epilogue warp: publishes results with release reductions; the CTA that
+//     finishes the router rows selects the top-k and publishes the routing
+//     record; the two halves of a gate/up item meet in shared memory, where h is
+//     rotated (H32) and quantized (Q8) without any round trip to other CTAs.
+// After its last item every CTA waits for all down items and combines a slice
+// of y in slot order: y = sum_s p_s o_s (+ o_shared).
+//
 // Sources: "DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
 // 395", section "ROCmFPX: fitting 284B weights into 128 GB" (read packed blocks
 // directly, expand small codebooks in registers, integer dot products, decode
@@ -38,12 +45,17 @@ namespace moeq {
 namespace {
 
 constexpr int kComputeWarps = 16;
+constexpr int kGroups = 2;  // compute groups on alternate stage fills
+constexpr int kGroupWarps = kComputeWarps / kGroups;
 constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kThreads = kComputeThreads + 32;
+constexpr int kProducerWarp = kComputeWarps;
+constexpr int kEpilogueWarp = kComputeWarps + 1;
+constexpr int kThreads = kComputeThreads + 64;
 constexpr int kStages = 3;
+constexpr int kEpi = 8;  // depth of the compute -> epilogue queue
 constexpr int kStageBytes = 68 * 1024;
-constexpr int kRouterRows = 8;
-constexpr int kGuRows = 16;
+constexpr int kRouterRows = 4;
+constexpr int kGuRows = 16;  // rows per gate/up fill; an item is two fills (one 32-block of h)
 constexpr int kDownRows = 32;
 constexpr int kMaxH = 4096;
 constexpr int kMaxB = kMaxH / 32 / 32;  // 32-blocks per lane along K
@@ -53,9 +65,16 @@ constexpr int kBarCompute = 1;  // named barrier of the compute warps
 
 enum UnitKind { U_ROUTER = 0, U_SGU, U_GU, U_SDOWN, U_DOWN, U_END };
 
+// One stage fill: kind, slot (0..k-1 routed, k shared), row chunk of its size.
 struct Unit {
   int kind, slot, chunk;
 };
+
+__device__ __forceinline__ int pack_unit(const Unit& u) { return (u.kind << 28) | (u.slot << 20) | u.chunk; }
+__device__ __forceinline__ Unit unpack_unit(int v) {
+  if (v < 0) return Unit{U_END, 0, 0};
+  return Unit{(v >> 28) & 15, (v >> 20) & 255, v & 0xfffff};
+}
 
 struct DecodeArgs {
   int H, I, E, k, nslots, has_shared;
@@ -67,13 +86,14 @@ struct DecodeArgs {
   float* y;
   uint32_t* ctr;
   float* logits;
-  float* hbuf;
   int8_t* hq;
-  uint16_t* hd;
+  uint8_t* hd;  // per slot, hd_stride bytes of fp16
+  int hd_stride;
   float* obuf;
   int32_t* status;
   moeq_debug dbg;
-  int nR, nSG, nGU, nSD, nD, total;
+  int nR, nSG, nGU, nSD, nD, items;  // item counts per kind and in total
+  int route_base, n_ctr;             // counter word offsets (moeq_layout.h)
 };
 
 struct alignas(128) DecodeSmem {
@@ -83,126 +103,182 @@ struct alignas(128) DecodeSmem {
   float xd[kMaxH / 32];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t epi_full[kEpi];
+  uint64_t epi_empty[kEpi];
   int unit[kStages];
+  int epi_unit[kEpi];
+  float hs[kEpi][kGuRows];          // h of a gate/up fill, per epilogue entry
+  uint32_t slot_cb[kMaxK + 1][12];  // codebooks of each slot's expert: gate, up, down
   int idx[kMaxK];
   float p[kMaxK];
+  int have_route;
   int last_cta;
-  int issued;    // stage fills issued by the producer
-  int consumed;  // stage fills waited for by the compute warps
+  int issued;             // stage fills issued by the producer
+  int consumed[kGroups];  // last stage fill waited for by each compute group
 };
 
-__device__ __forceinline__ Unit unit_of(const DecodeArgs& a, int u) {
-  Unit r{U_END, 0, 0};
-  if (u < 0) return r;
-  if (u < a.nR) return Unit{U_ROUTER, 0, u};
-  u -= a.nR;
-  if (u < a.nSG) return Unit{U_SGU, a.k, u};
-  u -= a.nSG;
-  const int gu_per_slot = a.I / kGuRows;
-  if (u < a.nGU) return Unit{U_GU, u / gu_per_slot, u % gu_per_slot};
-  u -= a.nGU;
-  if (u < a.nSD) return Unit{U_SDOWN, a.k, u};
-  u -= a.nSD;
-  const int d_per_slot = a.H / kDownRows;
-  if (u < a.nD) return Unit{U_DOWN, u / d_per_slot, u % d_per_slot};
-  return r;
+// Item -> its first fill and number of fills.
+__device__ __forceinline__ int item_fills(const DecodeArgs& a, int i, Unit& first) {
+  if (i < 0 || i >= a.items) return 0;
+  if (i < a.nR) { first = Unit{U_ROUTER, 0, i}; return 1; }
+  i -= a.nR;
+  if (i < a.nSG) { first = Unit{U_SGU, a.k, 2 * i}; return 2; }
+  i -= a.nSG;
+  if (i < a.nSD) { first = Unit{U_SDOWN, a.k, i}; return 1; }
+  i -= a.nSD;
+  const int pairs = a.I / (2 * kGuRows);
+  if (i < a.nGU) { first = Unit{U_GU, i / pairs, 2 * (i % pairs)}; return 2; }
+  i -= a.nGU;
+  const int per = a.H / kDownRows;
+  first = Unit{U_DOWN, i / per, i % per};
+  return 1;
 }
 
-// Byte offsets inside a stage: [codes A][scales A][codes B][scales B].
+// Byte offsets inside a stage. Gate/up: [codes G][scales G][codes U][scales U].
+// Down: [codes][scales][hq of the slot][hd of the slot].
 struct StageMap {
   uint32_t ca, sa, cb, sb, total;
 };
 
 __host__ __device__ __forceinline__ uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
 
+__host__ __device__ __forceinline__ uint32_t code_pitch(int fmt, int K) {
+  return static_cast<uint32_t>(K / 32) * (fmt == 2 ? 8 : fmt == 3 ? 12 : 16);
+}
+__host__ __device__ __forceinline__ uint32_t scale_pitch(int fmt, int K) {
+  return static_cast<uint32_t>(K / 32) * (fmt == 4 ? 1 : 2);
+}
+
 __host__ __device__ __forceinline__ StageMap gu_map(int fmt, int K) {
-  const int nb = K / 32;
-  const uint32_t c = kGuRows * nb * (fmt == 2 ? 8 : fmt == 3 ? 12 : 16);
-  const uint32_t s = al16(kGuRows * nb * (fmt == 4 ? 1 : 2));
+  const uint32_t c = kGuRows * code_pitch(fmt, K);
+  const uint32_t s = al16(kGuRows * scale_pitch(fmt, K));
   return StageMap{0, c, c + s, c + s + c, 2 * (c + s)};
 }
 
 __host__ __device__ __forceinline__ StageMap down_map(int fmt, int K) {
-  const int nb = K / 32;
-  const uint32_t c = kDownRows * nb * (fmt == 2 ? 8 : fmt == 3 ? 12 : 16);
-  const uint32_t s = al16(kDownRows * nb * (fmt == 4 ? 1 : 2));
-  return StageMap{0, c, 0, 0, c + s};
-}
-
-// ------------------------------------------------------------------ producer side
-__device__ void producer_topk(const DecodeArgs& a, DecodeSmem& sm, int lane) {
-  if (lane == 0 && !spin_until_geq(&a.ctr[1], static_cast<uint32_t>(a.nR)))
-    set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
-  __syncwarp();
-  const int nper = (a.E + 31) / 32;
-  float v[kMaxEPerLane];
-  uint32_t valid = 0;
-#pragma unroll
-  for (int i = 0; i < kMaxEPerLane; ++i) {
-    const bool ok = i < nper && lane + 32 * i < a.E;
-    v[i] = ok ? __ldcg(&a.logits[lane + 32 * i]) : 0.0f;
-    valid |= (ok ? 1u : 0u) << i;
-  }
-  uint32_t taken = 0;
-  int sel[kMaxK];
-  float selv[kMaxK];
-#pragma unroll
-  for (int s = 0; s < kMaxK; ++s) {
-    sel[s] = 0;
-    selv[s] = 0.0f;
-    if (s >= a.k) continue;
-    float bv = 0.0f;
-    int bi = -1;
-#pragma unroll
-    for (int i = 0; i < kMaxEPerLane; ++i) {
-      if (!((valid >> i) & 1u) || ((taken >> i) & 1u)) continue;
-      const int e = lane + 32 * i;
-      if (bi < 0 || ranks_before(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sel[s] = bi;
-    selv[s] = bv;
-  }
-  // softmax over all E logits at the selected indices (max = the first selected)
-  const float m = selv[0];
-  float z = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kMaxEPerLane; ++i)
-    if (((valid >> i) & 1u) && !isnan(v[i])) z += expf(v[i] - m);
-  z = warp_sum_canonical(z);
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < kMaxK; ++s) {
-      if (s >= a.k) continue;
-      const float ps = __fdiv_rn(expf(selv[s] - m), z);
-      sm.idx[s] = sel[s];
-      sm.p[s] = ps;
-      if (blockIdx.x == 0) {
-        if (a.dbg.idx) a.dbg.idx[s] = sel[s];
-        if (a.dbg.p) a.dbg.p[s] = ps;
-      }
-    }
-  }
-  __syncwarp();
+  const uint32_t c = kDownRows * code_pitch(fmt, K);
+  const uint32_t s = al16(kDownRows * scale_pitch(fmt, K));
+  const uint32_t hq = static_cast<uint32_t>(K);
+  const uint32_t hd = al16(2 * static_cast<uint32_t>(K / 32));
+  return StageMap{0, c, c + s, c + s + hq, c + s + hq + hd};
 }
 
 __device__ __forceinline__ const DMat& gu_mat(const DecodeArgs& a, bool shared, bool up) {
   return shared ? (up ? a.sup : a.sgate) : (up ? a.up : a.gate);
 }
 
-// Issues the copies of unit un into stage s (lane 0 of the producer warp).
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Appends one timeline event of a role of this CTA (debug only).
+__device__ __forceinline__ void trace_ev(const DecodeArgs& a, int role, int& n, uint32_t ev, int unit) {
+  if (a.dbg.trace && n < a.dbg.trace_cap) {
+    uint64_t* p = a.dbg.trace + 2 * ((static_cast<size_t>(blockIdx.x) * 4 + role) * a.dbg.trace_cap + n);
+    p[0] = global_ns();
+    p[1] = (static_cast<uint64_t>(ev) << 32) | static_cast<uint32_t>(unit);
+  }
+  ++n;
+}
+
+// ------------------------------------------------------------------ routing
+// Top-k of the router logits and softmax weights by one warp, then the
+// routing record, written to kRouteCopies lines, and the ready flag. Runs in
+// the epilogue warp of the CTA that completes the router rows.
+template <int NPL>
+__device__ void route_topk(const DecodeArgs& a, int lane, int& my_idx, float& ps, int& ntr) {
+  float v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < a.E ? __ldcg(&a.logits[e]) : 0.0f;
+  }
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) sum += v[i];
+  if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 3000 + (sum != sum ? 1 : 0));
+  warp_topk<NPL>(v, a.E, a.k, lane, my_idx, ps);
+  if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 3001 + (ps != ps ? 1 : 0));
+}
+
+__device__ void route_and_publish(const DecodeArgs& a, int lane, int& ntr) {
+  int my_idx;
+  float ps;
+  if (a.E <= 256) route_topk<8>(a, lane, my_idx, ps, ntr);
+  else route_topk<kMaxEPerLane>(a, lane, my_idx, ps, ntr);
+  if (lane < a.k) {
+    if (a.dbg.idx) a.dbg.idx[lane] = my_idx;
+    if (a.dbg.p) a.dbg.p[lane] = ps;
+  }
+  // lanes 0..7 write idx, lanes 8..15 write p, into every copy
+  const float pl = __shfl_sync(0xffffffffu, ps, lane & 7);
+  const uint32_t word = lane < 8 ? static_cast<uint32_t>(my_idx) : __float_as_uint(pl);
+  if (lane < 16 && (lane & 7) < a.k)
+    for (int c = 0; c < kRouteCopies; ++c) a.ctr[a.route_base + kCtrLine * c + lane] = word;
+  __syncwarp();
+  if (lane == 0) red_add_release(&a.ctr[kCtrRouteReady], 1u);
+  if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 3002);
+}
+
+// Waits for the routing record and loads this CTA's copy (one warp).
+__device__ void fetch_route(const DecodeArgs& a, DecodeSmem& sm, int lane) {
+  if (lane == 0 && !spin_until_geq(&a.ctr[kCtrRouteReady], 1u)) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+  __syncwarp();
+  const uint32_t* rec = a.ctr + a.route_base + kCtrLine * (blockIdx.x % kRouteCopies);
+  if (lane < a.k) {
+    sm.idx[lane] = static_cast<int>(__ldcg(rec + lane));
+    sm.p[lane] = __uint_as_float(__ldcg(rec + 8 + lane));
+  }
+  __syncwarp();
+}
+
+// Codebooks of a slot's expert (gate, up, down) into shared memory.
+__device__ __forceinline__ void load_cb_words(const DMat& m, int e, uint32_t* w) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(m.cb + static_cast<size_t>(e) * m.cb_stride);
+  const int n = (1 << m.fmt) / 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = i < n ? __ldg(p + i) : 0u;
+}
+
+__device__ void stage_slot_cb(const DecodeArgs& a, DecodeSmem& sm, int slot) {
+  const bool shared = slot == a.k;
+  const int e = shared ? 0 : sm.idx[slot];
+  load_cb_words(shared ? a.sgate : a.gate, e, sm.slot_cb[slot]);
+  load_cb_words(shared ? a.sup : a.up, e, sm.slot_cb[slot] + 4);
+  load_cb_words(shared ? a.sdown : a.down, e, sm.slot_cb[slot] + 8);
+}
+
+// ------------------------------------------------------------------ producer side
+// Source ranges of the down rows of (slot, chunk).
+__device__ __forceinline__ void down_src(const DecodeArgs& a, const DecodeSmem& sm, int slot,
+                                         int chunk, const uint8_t*& c, uint32_t& cbytes,
+                                         const uint8_t*& s, uint32_t& sbytes) {
+  const bool shared = slot == a.k;
+  const DMat& D = shared ? a.sdown : a.down;
+  const int e = shared ? 0 : sm.idx[slot];
+  const size_t pc = code_pitch(D.fmt, a.I), ps = scale_pitch(D.fmt, a.I);
+  const size_t r0 = static_cast<size_t>(chunk) * kDownRows;
+  c = D.codes + e * D.stride_codes + r0 * pc;
+  s = D.scales + e * D.stride_scales + r0 * ps;
+  cbytes = static_cast<uint32_t>(kDownRows * pc);
+  sbytes = static_cast<uint32_t>(kDownRows * ps);
+}
+
+// L2 prefetch of this CTA's share of the down rows of slots [slot_lo, slot_hi).
+__device__ void prefetch_down(const DecodeArgs& a, const DecodeSmem& sm, int slot_lo, int slot_hi) {
+  const int per = a.H / kDownRows;
+  for (int j = blockIdx.x; j < (slot_hi - slot_lo) * per; j += gridDim.x) {
+    const uint8_t *c, *s;
+    uint32_t cb, sb;
+    down_src(a, sm, slot_lo + j / per, j % per, c, cb, s, sb);
+    bulk_prefetch_l2(c, cb);
+    bulk_prefetch_l2(s, sb);
+  }
+}
+
+// Issues the copies of fill un into stage s (lane 0 of the producer warp).
 __device__ void issue_unit(const DecodeArgs& a, DecodeSmem& sm, int s, const Unit& un) {
   uint8_t* st = sm.stage[s];
   uint64_t* bar = &sm.full[s];
@@ -217,12 +293,11 @@ __device__ void issue_unit(const DecodeArgs& a, DecodeSmem& sm, int s, const Uni
     const DMat& G = gu_mat(a, shared, false);
     const DMat& U = gu_mat(a, shared, true);
     const int e = shared ? 0 : sm.idx[un.slot];
-    const int nb = a.H / 32;
-    const size_t pc = static_cast<size_t>(nb) * (G.fmt == 2 ? 8 : G.fmt == 3 ? 12 : 16);
-    const size_t ps = static_cast<size_t>(nb) * (G.fmt == 4 ? 1 : 2);
+    const size_t pc = code_pitch(G.fmt, a.H), ps = scale_pitch(G.fmt, a.H);
     const StageMap mp = gu_map(G.fmt, a.H);
     const size_t r0 = static_cast<size_t>(un.chunk) * kGuRows;
-    const uint32_t cbytes = static_cast<uint32_t>(kGuRows * pc), sbytes = static_cast<uint32_t>(kGuRows * ps);
+    const uint32_t cbytes = static_cast<uint32_t>(kGuRows * pc);
+    const uint32_t sbytes = static_cast<uint32_t>(kGuRows * ps);
     mbar_arrive_expect_tx(bar, 2 * (cbytes + sbytes));
     bulk_g2s(st + mp.ca, G.codes + e * G.stride_codes + r0 * pc, cbytes, bar);
     bulk_g2s(st + mp.sa, G.scales + e * G.stride_scales + r0 * ps, sbytes, bar);
@@ -230,242 +305,226 @@ __device__ void issue_unit(const DecodeArgs& a, DecodeSmem& sm, int s, const Uni
     bulk_g2s(st + mp.sb, U.scales + e * U.stride_scales + r0 * ps, sbytes, bar);
     return;
   }
-  if (un.kind == U_SDOWN || un.kind == U_DOWN) {
-    const bool shared = un.kind == U_SDOWN;
-    const DMat& D = shared ? a.sdown : a.down;
-    const int e = shared ? 0 : sm.idx[un.slot];
-    const int nb = a.I / 32;
-    const size_t pc = static_cast<size_t>(nb) * (D.fmt == 2 ? 8 : D.fmt == 3 ? 12 : 16);
-    const size_t ps = static_cast<size_t>(nb) * (D.fmt == 4 ? 1 : 2);
-    const StageMap mp = down_map(D.fmt, a.I);
-    const size_t r0 = static_cast<size_t>(un.chunk) * kDownRows;
-    const uint32_t cbytes = static_cast<uint32_t>(kDownRows * pc), sbytes = static_cast<uint32_t>(kDownRows * ps);
-    mbar_arrive_expect_tx(bar, cbytes + sbytes);
-    bulk_g2s(st + mp.ca, D.codes + e * D.stride_codes + r0 * pc, cbytes, bar);
-    bulk_g2s(st + mp.sa, D.scales + e * D.stride_scales + r0 * ps, sbytes, bar);
-    return;
-  }
+  // down fill: weights now, this slot's quantized h once it is complete
+  const DMat& D = un.kind == U_SDOWN ? a.sdown : a.down;
+  const StageMap mp = down_map(D.fmt, a.I);
+  const uint8_t *c, *sc;
+  uint32_t cbytes, sbytes;
+  down_src(a, sm, un.slot, un.chunk, c, cbytes, sc, sbytes);
+  const uint32_t hqb = static_cast<uint32_t>(a.I), hdb = static_cast<uint32_t>(a.hd_stride);
+  mbar_arrive_expect_tx(bar, cbytes + sbytes + hqb + hdb);
+  bulk_g2s(st + mp.ca, c, cbytes, bar);
+  bulk_g2s(st + mp.sa, sc, sbytes, bar);
+  if (!spin_until_geq(&a.ctr[kCtrHqDone + kCtrLine * un.slot], static_cast<uint32_t>(a.I / 32)))
+    set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  bulk_g2s(st + mp.cb, a.hq + static_cast<size_t>(un.slot) * a.I, hqb, bar);
+  bulk_g2s(st + mp.sb, a.hd + static_cast<size_t>(un.slot) * a.hd_stride, hdb, bar);
 }
 
 // ------------------------------------------------------------------ compute side
-__device__ __forceinline__ void load_cb(const DMat& m, int e, uint32_t* cb) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(m.cb + static_cast<size_t>(e) * m.cb_stride);
-  const int n = (1 << m.fmt) / 4;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) cb[i] = i < n ? __ldg(p + i) : 0u;
+__device__ __forceinline__ void load_q(const int8_t* p, int* q) {
+  const int4 q0 = *reinterpret_cast<const int4*>(p);
+  const int4 q1 = *reinterpret_cast<const int4*>(p + 16);
+  q[0] = q0.x; q[1] = q0.y; q[2] = q0.z; q[3] = q0.w;
+  q[4] = q1.x; q[5] = q1.y; q[6] = q1.z; q[7] = q1.w;
 }
 
-// One row of gate and up (same row index) against the quantized x in smem.
+// Rows r0 and r1 of the gate and up tiles in the stage against the quantized x
+// in shared memory: g[0], u[0] for r0 and g[1], u[1] for r1.
 template <int FMT>
-__device__ void gu_row(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t* st,
-                       const StageMap& mp, const uint32_t* cbg, const uint32_t* cbu, int r,
-                       int grow, int slot, int lane, float& g, float& u) {
+__device__ void gu_rows(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t* st,
+                        const uint32_t* cbg, const uint32_t* cbu, int r0, int r1, int row_base,
+                        int slot, int lane, float* g, float* u) {
   constexpr int BC = block_bytes<FMT>();
+  constexpr int SB = FMT == 4 ? 1 : 2;
+  const StageMap mp = gu_map(FMT, a.H);
   const int nb = a.H / 32;
-  const uint8_t* gc = st + mp.ca + r * nb * BC;
-  const uint8_t* uc = st + mp.cb + r * nb * BC;
-  const uint8_t* gs = st + mp.sa + r * nb * (FMT == 4 ? 1 : 2);
-  const uint8_t* us = st + mp.sb + r * nb * (FMT == 4 ? 1 : 2);
-  float ag = 0.0f, au = 0.0f;
+  const uint8_t* gc0 = st + mp.ca + r0 * nb * BC;
+  const uint8_t* gc1 = st + mp.ca + r1 * nb * BC;
+  const uint8_t* uc0 = st + mp.cb + r0 * nb * BC;
+  const uint8_t* uc1 = st + mp.cb + r1 * nb * BC;
+  const uint8_t* gs0 = st + mp.sa + r0 * nb * SB;
+  const uint8_t* gs1 = st + mp.sa + r1 * nb * SB;
+  const uint8_t* us0 = st + mp.sb + r0 * nb * SB;
+  const uint8_t* us1 = st + mp.sb + r1 * nb * SB;
+  float ag0 = 0.0f, au0 = 0.0f, ag1 = 0.0f, au1 = 0.0f;
 #pragma unroll
   for (int i = 0; i < kMaxB; ++i) {
     const int b = lane + 32 * i;
     if (b < nb) {
       int q[8];
-      const int4 q0 = *reinterpret_cast<const int4*>(sm.xq + 32 * b);
-      const int4 q1 = *reinterpret_cast<const int4*>(sm.xq + 32 * b + 16);
-      q[0] = q0.x; q[1] = q0.y; q[2] = q0.z; q[3] = q0.w;
-      q[4] = q1.x; q[5] = q1.y; q[6] = q1.z; q[7] = q1.w;
+      load_q(sm.xq + 32 * b, q);
       const float xd = sm.xd[b];
-      const int sg = block_dot<FMT>(gc + b * BC, cbg, q);
-      const int su = block_dot<FMT>(uc + b * BC, cbu, q);
-      ag = fmaf(block_scale<FMT>(gs, b) * xd, static_cast<float>(sg), ag);
-      au = fmaf(block_scale<FMT>(us, b) * xd, static_cast<float>(su), au);
-      if (a.dbg.S_gate) a.dbg.S_gate[(static_cast<size_t>(slot) * a.I + grow) * nb + b] = sg;
-      if (a.dbg.S_up) a.dbg.S_up[(static_cast<size_t>(slot) * a.I + grow) * nb + b] = su;
+      const int sg0 = block_dot<FMT>(gc0 + b * BC, cbg, q);
+      const int su0 = block_dot<FMT>(uc0 + b * BC, cbu, q);
+      const int sg1 = block_dot<FMT>(gc1 + b * BC, cbg, q);
+      const int su1 = block_dot<FMT>(uc1 + b * BC, cbu, q);
+      ag0 = fmaf(block_scale<FMT>(gs0, b) * xd, static_cast<float>(sg0), ag0);
+      au0 = fmaf(block_scale<FMT>(us0, b) * xd, static_cast<float>(su0), au0);
+      ag1 = fmaf(block_scale<FMT>(gs1, b) * xd, static_cast<float>(sg1), ag1);
+      au1 = fmaf(block_scale<FMT>(us1, b) * xd, static_cast<float>(su1), au1);
+      if (a.dbg.S_gate) {
+        a.dbg.S_gate[(static_cast<size_t>(slot) * a.I + row_base + r0) * nb + b] = sg0;
+        a.dbg.S_gate[(static_cast<size_t>(slot) * a.I + row_base + r1) * nb + b] = sg1;
+      }
+      if (a.dbg.S_up) {
+        a.dbg.S_up[(static_cast<size_t>(slot) * a.I + row_base + r0) * nb + b] = su0;
+        a.dbg.S_up[(static_cast<size_t>(slot) * a.I + row_base + r1) * nb + b] = su1;
+      }
     }
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) {
-    ag += __shfl_xor_sync(0xffffffffu, ag, d);
-    au += __shfl_xor_sync(0xffffffffu, au, d);
+    ag0 += __shfl_xor_sync(0xffffffffu, ag0, d);
+    au0 += __shfl_xor_sync(0xffffffffu, au0, d);
+    ag1 += __shfl_xor_sync(0xffffffffu, ag1, d);
+    au1 += __shfl_xor_sync(0xffffffffu, au1, d);
   }
-  g = ag;
-  u = au;
+  g[0] = ag0; u[0] = au0; g[1] = ag1; u[1] = au1;
 }
 
-// Two rows (r, r + 16) of a down matrix against the quantized h of one slot.
+// Rows wg, wg + 8, wg + 16, wg + 24 of the down tile in the stage against the
+// slot's quantized h, which the producer placed in the same stage.
 template <int FMT>
-__device__ void down_rows(const DecodeArgs& a, const uint8_t* st, const StageMap& mp,
-                          const uint32_t* cb, const int (*q)[8], const float* hdf, int warp,
+__device__ void down_rows(const DecodeArgs& a, const uint8_t* st, const uint32_t* cb, int wg,
                           int lane, int chunk, int slot, float* o) {
   constexpr int BC = block_bytes<FMT>();
+  constexpr int SB = FMT == 4 ? 1 : 2;
+  constexpr int R = kDownRows / kGroupWarps;
+  const StageMap mp = down_map(FMT, a.I);
   const int nb = a.I / 32;
+  const int8_t* hq = reinterpret_cast<const int8_t*>(st + mp.cb);
+  const uint16_t* hd = reinterpret_cast<const uint16_t*>(st + mp.sb);
+  float acc[R];
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int r = warp + 16 * rr;
-    const uint8_t* c = st + mp.ca + r * nb * BC;
-    const uint8_t* sc = st + mp.sa + r * nb * (FMT == 4 ? 1 : 2);
-    float acc = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kMaxB; ++i) {
-      const int b = lane + 32 * i;
-      if (b < nb) {
-        const int sd = block_dot<FMT>(c + b * BC, cb, q[i]);
-        acc = fmaf(block_scale<FMT>(sc, b) * hdf[i], static_cast<float>(sd), acc);
-        if (a.dbg.S_down)
-          a.dbg.S_down[(static_cast<size_t>(slot) * a.H + chunk * kDownRows + r) * nb + b] = sd;
-      }
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
-    o[rr] = acc;
-  }
-}
-
-__device__ void router_unit(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t* st,
-                            int chunk, int warp, int lane) {
-  if (warp < kRouterRows) {
-    const int e = chunk * kRouterRows + warp;
-    const uint8_t* wrow = st + static_cast<size_t>(warp) * a.H * 2;
-    float acc = 0.0f;
-    for (int i = 0; i < a.H / 256; ++i) {
-      const int k0 = 256 * i + 8 * lane;
-      const uint4 w = *reinterpret_cast<const uint4*>(wrow + 2 * k0);
-      const uint4 x = *reinterpret_cast<const uint4*>(sm.xb + k0);
-      acc = fmaf(bf16_lo(x.x), bf16_lo(w.x), acc);
-      acc = fmaf(bf16_hi(x.x), bf16_hi(w.x), acc);
-      acc = fmaf(bf16_lo(x.y), bf16_lo(w.y), acc);
-      acc = fmaf(bf16_hi(x.y), bf16_hi(w.y), acc);
-      acc = fmaf(bf16_lo(x.z), bf16_lo(w.z), acc);
-      acc = fmaf(bf16_hi(x.z), bf16_hi(w.z), acc);
-      acc = fmaf(bf16_lo(x.w), bf16_lo(w.w), acc);
-      acc = fmaf(bf16_hi(x.w), bf16_hi(w.w), acc);
-    }
-    acc = warp_sum_canonical(acc);
-    if (lane == 0) {
-      a.logits[e] = acc;
-      if (a.dbg.logits) a.dbg.logits[e] = acc;
-    }
-  }
-  named_bar(kBarCompute, kComputeThreads);
-  if (warp == 0 && lane == 0) {
-    __threadfence();
-    atomicAdd(&a.ctr[1], 1u);
-  }
-}
-
-template <int FMT>
-__device__ void gu_unit(const DecodeArgs& a, DecodeSmem& sm, const uint8_t* st, const Unit& un,
-                        int warp, int lane) {
-  const bool shared = un.kind == U_SGU;
-  const DMat& G = gu_mat(a, shared, false);
-  const DMat& U = gu_mat(a, shared, true);
-  const int e = shared ? 0 : sm.idx[un.slot];
-  uint32_t cbg[4], cbu[4];
-  load_cb(G, e, cbg);
-  load_cb(U, e, cbu);
-  const StageMap mp = gu_map(FMT, a.H);
-  const int grow = un.chunk * kGuRows + warp;
-  float g, u;
-  gu_row<FMT>(a, sm, st, mp, cbg, cbu, warp, grow, un.slot, lane, g, u);
-  if (lane == 0) {
-    const float h = g * u / (1.0f + expf(-g));
-    a.hbuf[static_cast<size_t>(un.slot) * a.I + grow] = h;
-    if (a.dbg.h) a.dbg.h[static_cast<size_t>(un.slot) * a.I + grow] = h;
-  }
-  named_bar(kBarCompute, kComputeThreads);
-  if (warp == 0) {
-    // the second CTA to finish a half of this 32-row block quantizes the block
-    const int nbI = a.I / 32, blk = un.chunk / 2;
-    uint32_t old = 0;
-    if (lane == 0) {
-      __threadfence();
-      old = atomicAdd(&a.ctr[kPairBase + un.slot * nbI + blk], 1u);
-    }
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == 1) {
-      __threadfence();
-      const size_t base = static_cast<size_t>(un.slot) * a.I + 32 * blk;
-      float v = __ldcg(&a.hbuf[base + lane]);
-      if (a.signs_h) v = h32_warp(v, __ldg(&a.signs_h[blk]), lane);
-      uint16_t db;
-      const int8_t q = q8_warp(v, db);
-      a.hq[base + lane] = q;
-      if (lane == 0) a.hd[static_cast<size_t>(un.slot) * nbI + blk] = db;
-      if (a.dbg.hq) a.dbg.hq[base + lane] = q;
-      if (a.dbg.hd && lane == 0) a.dbg.hd[static_cast<size_t>(un.slot) * nbI + blk] = db;
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        atomicAdd(&a.ctr[kCtrHqDone + un.slot], 1u);
-      }
-    }
-  }
-}
-
-template <int FMT>
-__device__ void down_unit(const DecodeArgs& a, DecodeSmem& sm, const uint8_t* st, const Unit& un,
-                          int warp, int lane) {
-  const bool shared = un.kind == U_SDOWN;
-  const DMat& D = shared ? a.sdown : a.down;
-  const int e = shared ? 0 : sm.idx[un.slot];
-  const int nbI = a.I / 32;
-  if (warp == 0 && lane == 0 &&
-      !spin_until_geq(&a.ctr[kCtrHqDone + un.slot], static_cast<uint32_t>(nbI)))
-    set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
-  named_bar(kBarCompute, kComputeThreads);
-  __threadfence();
-  uint32_t cb[4];
-  load_cb(D, e, cb);
-  int q[kMaxB][8];
-  float hdf[kMaxB];
+  for (int j = 0; j < R; ++j) acc[j] = 0.0f;
 #pragma unroll
   for (int i = 0; i < kMaxB; ++i) {
     const int b = lane + 32 * i;
-    if (b < nbI) {
-      const size_t base = static_cast<size_t>(un.slot) * a.I + 32 * b;
-      const int4 q0 = __ldcg(reinterpret_cast<const int4*>(a.hq + base));
-      const int4 q1 = __ldcg(reinterpret_cast<const int4*>(a.hq + base + 16));
-      q[i][0] = q0.x; q[i][1] = q0.y; q[i][2] = q0.z; q[i][3] = q0.w;
-      q[i][4] = q1.x; q[i][5] = q1.y; q[i][6] = q1.z; q[i][7] = q1.w;
-      hdf[i] = f16_bits_to_f32(__ldcg(a.hd + static_cast<size_t>(un.slot) * nbI + b));
-    } else {
+    if (b < nb) {
+      int q[8];
+      load_q(hq + 32 * b, q);
+      const float hdf = f16_bits_to_f32(hd[b]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) q[i][j] = 0;
-      hdf[i] = 0.0f;
+      for (int j = 0; j < R; ++j) {
+        const int r = wg + kGroupWarps * j;
+        const int d = block_dot<FMT>(st + mp.ca + r * nb * BC + b * BC, cb, q);
+        acc[j] = fmaf(block_scale<FMT>(st + mp.sa + r * nb * SB, b) * hdf, static_cast<float>(d), acc[j]);
+        if (a.dbg.S_down)
+          a.dbg.S_down[(static_cast<size_t>(slot) * a.H + chunk * kDownRows + r) * nb + b] = d;
+      }
     }
   }
-  const StageMap mp = down_map(FMT, a.I);
-  float o[2];
-  down_rows<FMT>(a, st, mp, cb, q, hdf, warp, lane, un.chunk, un.slot, o);
-  if (lane == 0) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const size_t at = static_cast<size_t>(un.slot) * a.H + un.chunk * kDownRows + warp + 16 * rr;
-      a.obuf[at] = o[rr];
-      if (a.dbg.o) a.dbg.o[at] = o[rr];
-    }
+  for (int d = 16; d >= 1; d >>= 1) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], d);
   }
-  named_bar(kBarCompute, kComputeThreads);
-  if (warp == 0) {
-    const int nchunks = a.H / kDownRows;
-    uint32_t old = 0;
+#pragma unroll
+  for (int j = 0; j < R; ++j) o[j] = acc[j];
+}
+
+__device__ float router_row(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t* st, int r,
+                            int lane) {
+  const uint8_t* wrow = st + static_cast<size_t>(r) * a.H * 2;
+  float acc = 0.0f;
+  for (int i = 0; i < a.H / 256; ++i) {
+    const int k0 = 256 * i + 8 * lane;
+    const uint4 w = *reinterpret_cast<const uint4*>(wrow + 2 * k0);
+    const uint4 x = *reinterpret_cast<const uint4*>(sm.xb + k0);
+    acc = fmaf(bf16_lo(x.x), bf16_lo(w.x), acc);
+    acc = fmaf(bf16_hi(x.x), bf16_hi(w.x), acc);
+    acc = fmaf(bf16_lo(x.y), bf16_lo(w.y), acc);
+    acc = fmaf(bf16_hi(x.y), bf16_hi(w.y), acc);
+    acc = fmaf(bf16_lo(x.z), bf16_lo(w.z), acc);
+    acc = fmaf(bf16_hi(x.z), bf16_hi(w.z), acc);
+    acc = fmaf(bf16_lo(x.w), bf16_lo(w.w), acc);
+    acc = fmaf(bf16_hi(x.w), bf16_hi(w.w), acc);
+  }
+  return warp_sum_canonical(acc);
+}
+
+// Computes fill un from stage s with the 8 warps of one compute group (wg =
+// warp in group); releases the stage as soon as it is read; results go to
+// shared memory (h, for epilogue entry e) or global memory (logits, o).
+__device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int e, const Unit& un,
+                             int wg, int lane) {
+  const uint8_t* st = sm.stage[s];
+  if (un.kind == U_ROUTER) {
+    float l = 0.0f;
+    if (wg < kRouterRows) l = router_row(a, sm, st, wg, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    if (wg < kRouterRows && lane == 0) {
+      const int ex = un.chunk * kRouterRows + wg;
+      a.logits[ex] = l;
+      if (a.dbg.logits) a.dbg.logits[ex] = l;
+    }
+    return;
+  }
+  if (un.kind == U_SGU || un.kind == U_GU) {
+    const int fmt = un.kind == U_SGU ? a.sgate.fmt : a.gate.fmt;
+    uint32_t cbg[4], cbu[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      cbg[i] = sm.slot_cb[un.slot][i];
+      cbu[i] = sm.slot_cb[un.slot][4 + i];
+    }
+    const int base = un.chunk * kGuRows;
+    float g[2], u[2];
+    if (fmt == 2) gu_rows<2>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
+    else if (fmt == 3) gu_rows<3>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
+    else gu_rows<4>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
+    __syncwarp();
     if (lane == 0) {
-      __threadfence();
-      old = atomicAdd(&a.ctr[kPairBase + a.nslots * nbI + un.chunk], 1u);
+      mbar_arrive(&sm.empty[s]);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = wg + kGroupWarps * j;
+        const float h = g[j] * u[j] / (1.0f + expf(-g[j]));
+        sm.hs[e][r] = h;
+        if (a.dbg.h) a.dbg.h[static_cast<size_t>(un.slot) * a.I + base + r] = h;
+      }
     }
-    old = __shfl_sync(0xffffffffu, old, 0);
-    (void)nchunks;
-    if (old == static_cast<uint32_t>(a.nslots - 1)) {
-      __threadfence();
-      const int row = un.chunk * kDownRows + lane;
-      float acc = 0.0f;
-      for (int s = 0; s < a.k; ++s) acc = fmaf(sm.p[s], __ldcg(&a.obuf[static_cast<size_t>(s) * a.H + row]), acc);
-      if (a.has_shared) acc += __ldcg(&a.obuf[static_cast<size_t>(a.k) * a.H + row]);
-      a.y[row] = acc;
+    return;
+  }
+  const int fmt = un.kind == U_SDOWN ? a.sdown.fmt : a.down.fmt;
+  uint32_t cb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cb[i] = sm.slot_cb[un.slot][8 + i];
+  constexpr int R = kDownRows / kGroupWarps;
+  float o[R];
+  if (fmt == 2) down_rows<2>(a, st, cb, wg, lane, un.chunk, un.slot, o);
+  else if (fmt == 3) down_rows<3>(a, st, cb, wg, lane, un.chunk, un.slot, o);
+  else down_rows<4>(a, st, cb, wg, lane, un.chunk, un.slot, o);
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(&sm.empty[s]);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const size_t at = static_cast<size_t>(un.slot) * a.H + un.chunk * kDownRows + wg + kGroupWarps * j;
+      a.obuf[at] = o[j];
+      if (a.dbg.o) a.dbg.o[at] = o[j];
     }
   }
+}
+
+// ------------------------------------------------------------------ epilogue side
+// Quantizes one 32-block of h whose halves sit in epilogue entries e0, e1.
+__device__ void quantize_h_block(const DecodeArgs& a, const DecodeSmem& sm, int e0, int e1,
+                                 int slot, int blk, int lane) {
+  float v = lane < kGuRows ? sm.hs[e0][lane] : sm.hs[e1][lane - kGuRows];
+  if (a.signs_h) v = h32_warp(v, __ldg(&a.signs_h[blk]), lane);
+  uint16_t db;
+  const int8_t q = q8_warp(v, db);
+  const size_t base = static_cast<size_t>(slot) * a.I + 32 * blk;
+  a.hq[base + lane] = q;
+  if (lane == 0) reinterpret_cast<uint16_t*>(a.hd + static_cast<size_t>(slot) * a.hd_stride)[blk] = db;
+  if (a.dbg.hq) a.dbg.hq[base + lane] = q;
+  if (a.dbg.hd && lane == 0) a.dbg.hd[static_cast<size_t>(slot) * (a.I / 32) + blk] = db;
+  __syncwarp();
+  if (lane == 0) red_add_release(&a.ctr[kCtrHqDone + kCtrLine * slot], 1u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
@@ -476,49 +535,118 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kComputeWarps);
+      mbar_init(&sm.empty[s], kGroupWarps);
     }
+    for (int e = 0; e < kEpi; ++e) {
+      mbar_init(&sm.epi_full[e], kGroupWarps);
+      mbar_init(&sm.epi_empty[e], 1);
+    }
+    sm.issued = 0;
+    sm.have_route = 0;
+    for (int g = 0; g < kGroups; ++g) sm.consumed[g] = g - kGroups;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kComputeWarps) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer warp
-    bool have_topk = false;
-    int it = 0;
-    for (;; ++it) {
-      const int s = it % kStages;
-      if (it >= kStages) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&sm.empty[s], ((it / kStages) - 1) & 1);
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-          set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
-          break;
-        }
-      }
-      int u = 0;
-      if (lane == 0) u = static_cast<int>(atomicAdd(&a.ctr[0], 1u));
-      u = __shfl_sync(0xffffffffu, u, 0);
-      const Unit un = unit_of(a, u);
-      if (un.kind == U_END) {
-        if (lane == 0) {
-          sm.unit[s] = -1;
-          mbar_arrive(&sm.full[s]);
-        }
-        ++it;
-        break;
-      }
-      if (!have_topk && un.kind != U_ROUTER && un.kind != U_SGU) {
-        producer_topk(a, sm, lane);
-        have_topk = true;
-      }
+    if (lane == 0 && a.has_shared) {
+      stage_slot_cb(a, sm, a.k);
+      prefetch_down(a, sm, a.k, a.k + 1);
+    }
+    __syncwarp();
+    int it = 0, ntr = 0;
+    bool aborted = false;
+    for (;;) {
+      int item = 0;
       if (lane == 0) {
-        sm.unit[s] = u;
-        issue_unit(a, sm, s, un);
+        item = static_cast<int>(atom_add_relaxed(&a.ctr[kCtrQueue], 1u));
+        trace_ev(a, 1, ntr, MOEQ_TRACE_TAKE, item);
       }
-      __syncwarp();
+      item = __shfl_sync(0xffffffffu, item, 0);
+      Unit first{U_END, 0, 0};
+      const int nf = item_fills(a, item, first);
+      if (nf > 0 && (first.kind == U_GU || first.kind == U_DOWN) && !sm.have_route) {
+        fetch_route(a, sm, lane);
+        if (lane < a.k) stage_slot_cb(a, sm, lane);
+        __syncwarp();
+        if (lane == 0) {
+          sm.have_route = 1;
+          trace_ev(a, 1, ntr, MOEQ_TRACE_TOPK, item);
+          prefetch_down(a, sm, 0, a.k);
+        }
+        __syncwarp();
+      }
+      // nf == 0: one end marker per compute group, on consecutive fills
+      const int fills = nf > 0 ? nf : kGroups;
+      for (int f = 0; f < fills; ++f, ++it) {
+        const int s = it % kStages;
+        if (it >= kStages) {
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait(&sm.empty[s], ((it / kStages) - 1) & 1);
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+            set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+            aborted = true;
+            break;
+          }
+        }
+        if (lane == 0) {
+          if (nf == 0) {
+            sm.unit[s] = -1;
+            mbar_arrive(&sm.full[s]);
+          } else {
+            Unit un = first;
+            un.chunk += f;
+            sm.unit[s] = pack_unit(un);
+            issue_unit(a, sm, s, un);
+            trace_ev(a, 1, ntr, MOEQ_TRACE_ISSUED, item);
+          }
+        }
+        __syncwarp();
+      }
+      if (aborted || nf == 0) break;
     }
     if (lane == 0) sm.issued = it;
+  } else if (warp == kEpilogueWarp) {
+    // ---------------------------------------------------------------- epilogue warp
+    int ntr = 0;
+    for (int n = 0;; ++n) {
+      const int e = n % kEpi;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&sm.epi_full[e], (n / kEpi) & 1);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+        set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      const Unit un = unpack_unit(sm.epi_unit[e]);
+      if (un.kind == U_END) break;
+      if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_EPI_BEGIN, pack_unit(un));
+      bool release = true;
+      if (un.kind == U_ROUTER) {
+        uint32_t old = 0;
+        if (lane == 0) old = atom_add_acq_rel(&a.ctr[kCtrRouter], 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        __syncwarp();
+        if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 2999);
+        if (old == static_cast<uint32_t>(a.nR - 1)) route_and_publish(a, lane, ntr);
+      } else if (un.kind == U_SGU || un.kind == U_GU) {
+        if ((un.chunk & 1) == 0) {
+          release = false;  // first half: its h waits in sm.hs[e] for the second half
+        } else {
+          const int ep = (n + kEpi - 1) % kEpi;
+          quantize_h_block(a, sm, ep, e, un.slot, un.chunk / 2, lane);
+          if (lane == 0) mbar_arrive(&sm.epi_empty[ep]);
+        }
+      } else {
+        __syncwarp();
+        if (lane == 0) red_add_release(&a.ctr[kCtrDownDone], 1u);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (release) mbar_arrive(&sm.epi_empty[e]);
+        trace_ev(a, 2, ntr, MOEQ_TRACE_EPI_END, pack_unit(un));
+      }
+    }
   } else {
     // ---------------------------------------------------------------- compute warps
     const int nbH = a.H / 32;
@@ -544,66 +672,84 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       }
     }
     named_bar(kBarCompute, kComputeThreads);
+    const int grp = warp / kGroupWarps, wg = warp % kGroupWarps;
+    const int role = grp == 0 ? 0 : 3;
+    int ntr = 0;
+    if (wg == 0 && lane == 0) trace_ev(a, role, ntr, MOEQ_TRACE_START, 0);
 
-    int it = 0;
-    bool aborted = false;
-    for (;; ++it) {
+    for (int it = grp;; it += kGroups) {
       const int s = it % kStages;
+      const int e = it % kEpi;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&sm.full[s], (it / kStages) & 1);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      // one decision for all compute warps, so that a timeout never splits them
-      if (!named_bar_and(kBarCompute, kComputeThreads, ok)) {
-        if (tid == 0) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
-        aborted = true;
+      if (lane == 0) {
+        ok = mbar_wait(&sm.full[s], (it / kStages) & 1);
+        if (ok && it >= kEpi) ok = mbar_wait(&sm.epi_empty[e], ((it / kEpi) - 1) & 1);
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+        set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
         break;
       }
       const int u = sm.unit[s];
-      const Unit un = unit_of(a, u);
-      if (un.kind == U_END) break;
-      const uint8_t* st = sm.stage[s];
-      if (un.kind == U_ROUTER) {
-        router_unit(a, sm, st, un.chunk, warp, lane);
-      } else if (un.kind == U_SGU || un.kind == U_GU) {
-        const int fmt = un.kind == U_SGU ? a.sgate.fmt : a.gate.fmt;
-        if (fmt == 2) gu_unit<2>(a, sm, st, un, warp, lane);
-        else if (fmt == 3) gu_unit<3>(a, sm, st, un, warp, lane);
-        else gu_unit<4>(a, sm, st, un, warp, lane);
-      } else {
-        const int fmt = un.kind == U_SDOWN ? a.sdown.fmt : a.down.fmt;
-        if (fmt == 2) down_unit<2>(a, sm, st, un, warp, lane);
-        else if (fmt == 3) down_unit<3>(a, sm, st, un, warp, lane);
-        else down_unit<4>(a, sm, st, un, warp, lane);
+      if (wg == 0 && lane == 0) {
+        sm.consumed[grp] = it;
+        trace_ev(a, role, ntr, MOEQ_TRACE_READY, u);
+      }
+      const Unit un = unpack_unit(u);
+      if (un.kind != U_END) compute_unit(a, sm, s, e, un, wg, lane);
+      if (wg == 0 && lane == 0) {
+        trace_ev(a, role, ntr, MOEQ_TRACE_DONE, u);
+        sm.epi_unit[e] = u;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[s]);
+      if (lane == 0) mbar_arrive(&sm.epi_full[e]);
+      if (un.kind == U_END) break;
     }
-    if (tid == 0) sm.consumed = aborted ? it - 1 : it;  // last fill waited for
   }
 
   // ---------------------------------------------------------------- teardown
   __syncthreads();
-  if (warp == kComputeWarps && lane == 0) {
-    // copies issued but never waited for (only after a timeout): let them land
-    for (int j = sm.consumed + 1; j < sm.issued; ++j)
-      if (!mbar_wait(&sm.full[j % kStages], (j / kStages) & 1)) break;
+  if (warp == kProducerWarp && lane == 0) {
+    // fills issued but never waited for (only after a timeout): let them land
+    for (int g = 0; g < kGroups; ++g)
+      for (int j = sm.consumed[g] + kGroups; j < sm.issued; j += kGroups)
+        if (!mbar_wait(&sm.full[j % kStages], (j / kStages) & 1)) break;
+  }
+  // combine y in slot order once every down item is done; 32 rows per warp
+  const int nchunks = a.H / kDownRows;
+  constexpr int kWarps = kThreads / 32;
+  if (static_cast<int>(blockIdx.x) * kWarps < nchunks) {
+    if (warp == 0) {
+      if (lane == 0 && !spin_until_geq(&a.ctr[kCtrDownDone], static_cast<uint32_t>(a.nSD + a.nD)))
+        set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+      __syncwarp();
+      if (!sm.have_route) fetch_route(a, sm, lane);
+    }
+    __syncthreads();
+    const int c = static_cast<int>(blockIdx.x) * kWarps + warp;
+    if (c < nchunks) {
+      const int row = c * kDownRows + lane;
+      float acc = 0.0f;
+      for (int s = 0; s < a.k; ++s)
+        acc = fmaf(sm.p[s], __ldcg(&a.obuf[static_cast<size_t>(s) * a.H + row]), acc);
+      if (a.has_shared) acc += __ldcg(&a.obuf[static_cast<size_t>(a.k) * a.H + row]);
+      a.y[row] = acc;
+    }
   }
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    const uint32_t old = atomicAdd(&a.ctr[2], 1u);
+    const uint32_t old = atomicAdd(&a.ctr[kCtrDone], 1u);
     sm.last_cta = old == gridDim.x - 1;
     if (sm.last_cta) __threadfence();
   }
   __syncthreads();
   if (sm.last_cta) {
-    const int n = kPairBase + a.nslots * (a.I / 32) + a.H / kDownRows;
-    for (int i = tid; i < n; i += kThreads)
-      if (i != 2) a.ctr[i] = 0u;
+    for (int i = tid; i < a.n_ctr; i += kThreads)
+      if (i != kCtrDone) a.ctr[i] = 0u;
     __syncthreads();
     if (tid == 0) {
       __threadfence();
-      a.ctr[2] = 0u;
+      a.ctr[kCtrDone] = 0u;
     }
   }
 }
@@ -611,7 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 }  // namespace
 
 bool decode_supported(const moeq_layer* L) {
-  if (L->H > kMaxH || L->I > kMaxH || L->E > kMaxE || L->E % kRouterRows || L->k > kMaxK) return false;
+  if (L->H > kMaxH || L->I > kMaxH || L->E > kMaxE || L->E % kRouterRows || L->k > kMaxK)
+    return false;
   if (static_cast<long>(kRouterRows) * L->H * 2 > kStageBytes) return false;
   if (gu_map(L->gate.fmt, L->H).total > static_cast<uint32_t>(kStageBytes)) return false;
   if (down_map(L->down.fmt, L->I).total > static_cast<uint32_t>(kStageBytes)) return false;
@@ -653,18 +800,20 @@ extern "C" int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, 
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.ctr = reinterpret_cast<uint32_t*>(w + wl.ctr);
   a.logits = reinterpret_cast<float*>(w + wl.logits);
-  a.hbuf = reinterpret_cast<float*>(w + wl.hbuf);
   a.hq = reinterpret_cast<int8_t*>(w + wl.hq);
-  a.hd = reinterpret_cast<uint16_t*>(w + wl.hd);
+  a.hd = w + wl.hd;
+  a.hd_stride = static_cast<int>(hd_stride(L->I));
   a.obuf = reinterpret_cast<float*>(w + wl.obuf);
   a.status = dev_status;
   if (dbg) a.dbg = *dbg;
   a.nR = L->E / kRouterRows;
-  a.nSG = a.has_shared ? L->I / kGuRows : 0;
-  a.nGU = L->k * (L->I / kGuRows);
+  a.nSG = a.has_shared ? L->I / (2 * kGuRows) : 0;
+  a.nGU = L->k * (L->I / (2 * kGuRows));
   a.nSD = a.has_shared ? L->H / kDownRows : 0;
   a.nD = L->k * (L->H / kDownRows);
-  a.total = a.nR + a.nSG + a.nGU + a.nSD + a.nD;
+  a.items = a.nR + a.nSG + a.nGU + a.nSD + a.nD;
+  a.route_base = route_base(a.nslots);
+  a.n_ctr = static_cast<int>(wl.n_ctr);
 
   const DeviceInfo& di = device_info();
   const size_t smem = sizeof(DecodeSmem);

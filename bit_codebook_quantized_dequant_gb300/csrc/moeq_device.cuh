@@ -99,9 +99,28 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 __device__ __forceinline__ bool spin_until_geq(const uint32_t* p, uint32_t target) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (ld_acquire(p) >= target) return true;
-    if (i > 8) __nanosleep(64);
+    __nanosleep(i < 4 ? 32 : 200);
   }
   return false;
+}
+
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Reduction add with release semantics at GPU scope (no return value).
+__device__ __forceinline__ void red_add_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Atomic add without ordering (work queues); returns the old value.
+__device__ __forceinline__ uint32_t atom_add_relaxed(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ void named_bar(int id, int threads) {
@@ -336,12 +355,80 @@ __device__ __forceinline__ float warp_sum_canonical(float a) {
   return a;
 }
 
-// Top-k selection ordering: larger value first, lower index on ties, NaN last.
-__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
-  const bool na = isnan(a), nb = isnan(b);
-  if (na != nb) return nb;
-  if (!na && a != b) return a > b;
-  return ia < ib;
+// Top-k selection ordering: larger value first, lower index on ties, NaN last,
+// -0 equal to +0. ranks_key maps (value, index) to a 64-bit key whose unsigned
+// order is that ordering (0 is below every real key and marks "no element").
+__device__ __forceinline__ uint32_t ordered_bits(float v) {
+  if (isnan(v)) return 0u;
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float from_ordered_bits(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+__device__ __forceinline__ uint64_t ranks_key(float v, int index) {
+  return (static_cast<uint64_t>(ordered_bits(v)) << 32) | (0xffffffffu - static_cast<uint32_t>(index));
+}
+
+// Top-k of E values held NPL per lane (lane l holds elements l + 32 i in v[i])
+// and their softmax weights over all E: after the call lane s < k holds the
+// s-th selected index in idx and its weight exp(l_s - max) / sum exp(l - max)
+// in p. Each lane sorts its keys with a bitonic network; k rounds of a warp
+// maximum over the lanes' heads then pick the winners in order.
+template <int NPL>
+__device__ __forceinline__ void warp_topk(const float (&v)[NPL], int E, int k, int lane, int& idx,
+                                          float& p) {
+  uint64_t key[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? ranks_key(v[i], e) : 0ull;
+  }
+#pragma unroll
+  for (int k2 = 2; k2 <= NPL; k2 <<= 1) {
+#pragma unroll
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const bool desc = (i & k2) == 0;
+          const uint64_t a = key[i], b = key[l];
+          const bool swap = desc ? (a < b) : (a > b);
+          key[i] = swap ? b : a;
+          key[l] = swap ? a : b;
+        }
+      }
+    }
+  }
+  uint64_t mine = 0ull, first = 0ull;
+  for (int s = 0; s < k; ++s) {
+    uint64_t h = key[0];
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, h, d);
+      h = o > h ? o : h;
+    }
+    if (s == 0) first = h;
+    if (lane == s) mine = h;
+    if (key[0] == h) {  // the lane that held the winner moves to its next key
+#pragma unroll
+      for (int i = 0; i + 1 < NPL; ++i) key[i] = key[i + 1];
+      key[NPL - 1] = 0ull;
+    }
+  }
+  const float m = from_ordered_bits(static_cast<uint32_t>(first >> 32));
+  float z = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && !isnan(v[i])) z += expf(v[i] - m);
+  }
+  z = warp_sum_canonical(z);
+  idx = static_cast<int>(0xffffffffu - static_cast<uint32_t>(mine));
+  p = __fdiv_rn(expf(from_ordered_bits(static_cast<uint32_t>(mine >> 32)) - m), z);
 }
 
 }  // namespace moeq

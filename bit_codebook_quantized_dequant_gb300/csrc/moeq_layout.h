@@ -10,17 +10,34 @@ constexpr int kMaxTopK = 8;
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Counter words of the persistent decode / verify kernels.
-//   [0] unit queue  [1] router units done  [2] CTAs finished
-//   [8 + s] quantized 32-blocks of h done for slot s
-//   [kPairBase ...]  one word per (slot, 32-block of h): halves written
-//   [after pairs ...] one word per 32-row chunk of y: slot outputs written
-constexpr int kCtrHqDone = 8;
-constexpr int kPairBase = 48;
+// Counter words of the persistent decode / verify kernels. Every counter that
+// many CTAs poll or update has its own 128-byte line:
+//   kCtrQueue      work queue (items taken)
+//   kCtrRouter     router items done
+//   kCtrRouteReady 1 once the routing record is published
+//   kCtrDownDone   down units done
+//   kCtrDone       CTAs finished (the last one resets the counters)
+//   kCtrHqDone + kCtrLine * s   quantized 32-blocks of h of slot s
+// followed by kRouteCopies lines holding copies of the routing record
+// (idx[8] then p[8] as fp32 bits), each read by a few CTAs only.
+constexpr int kCtrLine = 32;  // words per 128-byte line
+constexpr int kCtrQueue = 0;
+constexpr int kCtrRouter = 1 * kCtrLine;
+constexpr int kCtrRouteReady = 2 * kCtrLine;
+constexpr int kCtrDownDone = 3 * kCtrLine;
+constexpr int kCtrDone = 4 * kCtrLine;
+constexpr int kCtrHqDone = 5 * kCtrLine;
+constexpr int kRouteCopies = 32;
+inline constexpr int route_base(int max_slots) { return kCtrHqDone + kCtrLine * max_slots; }
+inline constexpr int ctr_words(int max_slots) { return route_base(max_slots) + kCtrLine * kRouteCopies; }
+
+// Bytes between the fp16 scales of h of consecutive slots (16-byte multiple so
+// that one slot's scales can be moved with a bulk copy).
+inline size_t hd_stride(int I) { return (2 * static_cast<size_t>(I / 32) + 15) & ~static_cast<size_t>(15); }
 
 struct DecodeWs {
   int nslots;
-  size_t ctr, n_ctr, logits, hbuf, hq, hd, obuf, total;
+  size_t ctr, n_ctr, logits, hq, hd, obuf, total;
 };
 
 inline DecodeWs decode_ws_layout(int H, int I, int E, int k, int has_shared, int cols = 1) {
@@ -30,16 +47,14 @@ inline DecodeWs decode_ws_layout(int H, int I, int E, int k, int has_shared, int
   w.nslots = cols * (k + (has_shared ? 1 : 0));
   size_t off = 0;
   w.ctr = off;
-  w.n_ctr = kPairBase + static_cast<size_t>(w.nslots) * (I / 32) + static_cast<size_t>(cols) * (H / 32);
+  w.n_ctr = static_cast<size_t>(ctr_words(w.nslots));
   off += align256(4 * w.n_ctr);
   w.logits = off;
   off += align256(4 * static_cast<size_t>(cols) * E);
-  w.hbuf = off;
-  off += align256(4 * static_cast<size_t>(w.nslots) * I);
   w.hq = off;
   off += align256(static_cast<size_t>(w.nslots) * I);
   w.hd = off;
-  off += align256(2 * static_cast<size_t>(w.nslots) * (I / 32));
+  off += align256(hd_stride(I) * static_cast<size_t>(w.nslots));
   w.obuf = off;
   off += align256(4 * static_cast<size_t>(w.nslots) * H);
   w.total = off;

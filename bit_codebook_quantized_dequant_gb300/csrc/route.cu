@@ -20,70 +20,29 @@ namespace {
 
 constexpr int kRtTokens = 8;
 constexpr int kRtWarps = 16;
-constexpr int kRtMaxEPerLane = 32;  // E <= 1024
 
 // Top-k + softmax weights of one token by one warp from E logits in memory `l`.
-__device__ void warp_topk(const float* l, int E, int k, int lane, int32_t* idx_out,
-                          float* w_out) {
-  const int nper = (E + 31) / 32;
-  float v[kRtMaxEPerLane];
-  uint32_t valid = 0;
+template <int NPL>
+__device__ void token_topk(const float* l, int E, int k, int lane, int32_t* idx_out, float* w_out) {
+  float v[NPL];
 #pragma unroll
-  for (int i = 0; i < kRtMaxEPerLane; ++i) {
-    const bool ok = i < nper && lane + 32 * i < E;
-    v[i] = ok ? l[lane + 32 * i] : 0.0f;
-    valid |= (ok ? 1u : 0u) << i;
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? l[e] : 0.0f;
   }
-  uint32_t taken = 0;
-  int sel[kMaxK];
-  float selv[kMaxK];
-#pragma unroll
-  for (int s = 0; s < kMaxK; ++s) {
-    sel[s] = 0;
-    selv[s] = 0.0f;
-    if (s >= k) continue;
-    float bv = 0.0f;
-    int bi = -1;
-#pragma unroll
-    for (int i = 0; i < kRtMaxEPerLane; ++i) {
-      if (!((valid >> i) & 1u) || ((taken >> i) & 1u)) continue;
-      const int e = lane + 32 * i;
-      if (bi < 0 || ranks_before(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-      if (oi >= 0 && (bi < 0 || ranks_before(ov, oi, bv, bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sel[s] = bi;
-    selv[s] = bv;
-  }
-  const float m = selv[0];
-  float z = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kRtMaxEPerLane; ++i)
-    if (((valid >> i) & 1u) && !isnan(v[i])) z += expf(v[i] - m);
-  z = warp_sum_canonical(z);
+  int idx;
+  float p;
+  warp_topk<NPL>(v, E, k, lane, idx, p);
   if (lane < k) {
-    int my = 0;
-    float mv = 0.0f;
-#pragma unroll
-    for (int s = 0; s < kMaxK; ++s)
-      if (s == lane) {
-        my = sel[s];
-        mv = selv[s];
-      }
-    idx_out[lane] = my;
-    w_out[lane] = __fdiv_rn(expf(mv - m), z);
+    idx_out[lane] = idx;
+    w_out[lane] = p;
   }
+}
+
+__device__ void warp_topk_any(const float* l, int E, int k, int lane, int32_t* idx_out, float* w_out) {
+  if (E <= 256) token_topk<8>(l, E, k, lane, idx_out, w_out);
+  else if (E <= 512) token_topk<16>(l, E, k, lane, idx_out, w_out);
+  else token_topk<32>(l, E, k, lane, idx_out, w_out);
 }
 
 __global__ void __launch_bounds__(kRtWarps * 32) route_kernel(
@@ -137,8 +96,8 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_kernel(
   }
   __syncthreads();
   if (warp < nt)
-    warp_topk(ls + warp * E, E, k, lane, idx + static_cast<size_t>(t0 + warp) * k,
-              w + static_cast<size_t>(t0 + warp) * k);
+    warp_topk_any(ls + warp * E, E, k, lane, idx + static_cast<size_t>(t0 + warp) * k,
+                  w + static_cast<size_t>(t0 + warp) * k);
 }
 
 __global__ void h32_kernel(const float* __restrict__ in, float* out, int nblk,

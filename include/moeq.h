@@ -99,7 +99,25 @@ typedef struct {
   float* o;                     /* [T x slots x H] expert outputs before the combine */
   int32_t* S_gate, *S_up;       /* decode only: [slots x I x H/32] int32 block partials */
   int32_t* S_down;              /* decode only: [slots x H x I/32] */
+  uint64_t* trace;              /* decode only: timeline, [grid x 4 roles x trace_cap x 2]
+                                   of (globaltimer ns, event << 32 | unit); see MOEQ_TRACE_* */
+  int trace_cap;                /* events per (CTA, role) */
 } moeq_debug;
+
+/* Timeline events of moe_ffn_decode (role 0 = compute group 0, 1 = producer
+ * warp, 2 = epilogue warp, 3 = compute group 1). Unused entries stay as the
+ * caller left them. */
+enum {
+  MOEQ_TRACE_START = 1,      /* compute: x quantized; producer: first unit taken */
+  MOEQ_TRACE_TAKE = 2,       /* producer: unit taken from the queue */
+  MOEQ_TRACE_TOPK = 3,       /* producer: top-k known */
+  MOEQ_TRACE_ISSUED = 4,     /* producer: all copies of the unit issued */
+  MOEQ_TRACE_READY = 5,      /* compute: the unit's stage is full */
+  MOEQ_TRACE_DONE = 6,       /* compute: unit computed */
+  MOEQ_TRACE_EPI_BEGIN = 7,  /* epilogue: unit handed over */
+  MOEQ_TRACE_EPI_END = 8,    /* epilogue: results published */
+  MOEQ_TRACE_SPIN = 9        /* producer: routing wait; first the value seen, then the polls */
+};
 
 /* ---------------------------------------------------------------- sizes */
 
@@ -152,7 +170,8 @@ int moe_route_topk(const uint16_t* x, int T, const uint16_t* router, int E, int 
  * Geometric": fused matvec and sync-free MoE decode). ws: a workspace of
  * moe_ffn_workspace(L, 1, 0) bytes, zeroed once with moe_ffn_workspace_init;
  * calls that share a workspace must be ordered (same stream). dbg may be NULL.
- * Requires H, I <= 4096 and multiples of 256; k <= 8. */
+ * Requires H <= 4096 and a multiple of 256, I <= 4096 and a multiple of 128,
+ * E <= 512 and a multiple of 8; k <= 8. */
 int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, void* ws, size_t ws_bytes,
                    int32_t* dev_status, const moeq_debug* dbg, moeq_stream stream);
 
