@@ -4,14 +4,16 @@
 // Work items are taken from a global queue in dependency order:
 //   router rows (4 per item)
 //   -> shared-expert gate/up (32 rows per item, as two 16-row fills)
+//   -> routing (one item: top-k and softmax weights of the router logits)
+//   -> shared-expert down rows (32 per item)
 //   -> routed gate/up (32 rows per item, slot-major)
-//   -> shared down rows (32 per item) -> routed down rows (32, slot-major)
+//   -> routed down rows (32 per item, slot-major)
 //   -> (after every down item) the combine of y.
 // An item only waits on items with a smaller queue index, and every CTA is
 // resident (cooperative launch), so every wait ends; each is bounded anyway and
 // reports MOEQ_ERR_DEVICE_TIMEOUT into the status word if it runs out.
 //
-// Per CTA (18 warps):
+// Per CTA (17 warps):
 //   * producer warp: takes items, streams their packed rows (code plane and
 //     scale plane, contiguous per row range) from HBM into a 3-stage shared
 //     memory ring with bulk asynchronous copies; once the routing record is
@@ -20,14 +22,16 @@
 //     is complete and copies it into the stage next to the weights;
 //   * two compute groups of 8 warps, on alternate stage fills: expand codes in
 //     registers (byte permutes), take int8 dot products per 32-block (dp4a),
-//     apply the block scales in fp32, release the stage as soon as it is read,
-//     and hand the fill to the epilogue warp;
-//   * epilogue warp: publishes results with release reductions; the CTA that
-//     finishes the router rows selects the top-k and publishes the routing
-//     record; the two halves of a gate/up item meet in shared memory, where h is
-//     rotated (H32) and quantized (Q8) without any round trip to other CTAs.
-// After its last item every CTA waits for all down items and combines a slice
-// of y in slot order: y = sum_s p_s o_s (+ o_shared).
+//     apply the block scales in fp32, and release the stage as soon as it is
+//     read. They also do all of the kernel's control work, because they own the
+//     issue slots (a separate control warp, sharing a scheduler with busy
+//     compute warps, ran an order of magnitude slower): the two halves of a
+//     gate/up item meet through shared memory and the second group rotates
+//     (H32) and quantizes (Q8) the 32-block of h; results are published with
+//     release reductions; the routing item is a rank-based top-k over 256
+//     threads.
+// After its last item every CTA with a share of y waits for all down items and
+// combines its rows in slot order: y = sum_s p_s o_s (+ o_shared).
 //
 // Sources: "DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
 // 395", section "ROCmFPX: fitting 284B weights into 128 GB" (read packed blocks
@@ -47,12 +51,11 @@ namespace {
 constexpr int kComputeWarps = 16;
 constexpr int kGroups = 2;  // compute groups on alternate stage fills
 constexpr int kGroupWarps = kComputeWarps / kGroups;
+constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kProducerWarp = kComputeWarps;
-constexpr int kEpilogueWarp = kComputeWarps + 1;
-constexpr int kThreads = kComputeThreads + 64;
+constexpr int kThreads = kComputeThreads + 32;
 constexpr int kStages = 3;
-constexpr int kEpi = 8;  // depth of the compute -> epilogue queue
 constexpr int kStageBytes = 68 * 1024;
 constexpr int kRouterRows = 4;
 constexpr int kGuRows = 16;  // rows per gate/up fill; an item is two fills (one 32-block of h)
@@ -60,10 +63,10 @@ constexpr int kDownRows = 32;
 constexpr int kMaxH = 4096;
 constexpr int kMaxB = kMaxH / 32 / 32;  // 32-blocks per lane along K
 constexpr int kMaxE = 512;
-constexpr int kMaxEPerLane = kMaxE / 32;
-constexpr int kBarCompute = 1;  // named barrier of the compute warps
+constexpr int kBarCompute = 1;  // named barrier of all compute warps
+constexpr int kBarGroup = 2;    // named barriers 2, 3: one per compute group
 
-enum UnitKind { U_ROUTER = 0, U_SGU, U_GU, U_SDOWN, U_DOWN, U_END };
+enum UnitKind { U_ROUTER = 0, U_SGU, U_GU, U_SDOWN, U_DOWN, U_ROUTE, U_END };
 
 // One stage fill: kind, slot (0..k-1 routed, k shared), row chunk of its size.
 struct Unit {
@@ -92,7 +95,7 @@ struct DecodeArgs {
   float* obuf;
   int32_t* status;
   moeq_debug dbg;
-  int nR, nSG, nGU, nSD, nD, items;  // item counts per kind and in total
+  int nR, nSG, nSD, nGU, nD, items;  // item counts per kind (plus one routing item)
   int route_base, n_ctr;             // counter word offsets (moeq_layout.h)
 };
 
@@ -103,11 +106,13 @@ struct alignas(128) DecodeSmem {
   float xd[kMaxH / 32];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t epi_full[kEpi];
-  uint64_t epi_empty[kEpi];
   int unit[kStages];
-  int epi_unit[kEpi];
-  float hs[kEpi][kGuRows];          // h of a gate/up fill, per epilogue entry
+  uint64_t rkey[kMaxE];             // routing item: ranking keys
+  float rwarp[kGroupWarps];         // routing item: per-warp softmax partial sums
+  float hs_first[kGroups][kGuRows];   // h of a first-half gate/up fill, by group
+  float hs_second[kGroups][kGuRows];  // h of a second-half gate/up fill, by group
+  volatile int hs_seq[kGroups];       // fill index of the first half in hs_first[g]
+  volatile int hs_ack[kGroups];       // fill index of the first half last consumed from it
   uint32_t slot_cb[kMaxK + 1][12];  // codebooks of each slot's expert: gate, up, down
   int idx[kMaxK];
   float p[kMaxK];
@@ -124,6 +129,8 @@ __device__ __forceinline__ int item_fills(const DecodeArgs& a, int i, Unit& firs
   i -= a.nR;
   if (i < a.nSG) { first = Unit{U_SGU, a.k, 2 * i}; return 2; }
   i -= a.nSG;
+  if (i == 0) { first = Unit{U_ROUTE, 0, 0}; return 1; }
+  i -= 1;
   if (i < a.nSD) { first = Unit{U_SDOWN, a.k, i}; return 1; }
   i -= a.nSD;
   const int pairs = a.I / (2 * kGuRows);
@@ -183,45 +190,16 @@ __device__ __forceinline__ void trace_ev(const DecodeArgs& a, int role, int& n, 
   ++n;
 }
 
+// Bounded spin on a shared-memory word until it equals want.
+__device__ __forceinline__ bool smem_wait_eq(const volatile int* w, int want) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (*w == want) return true;
+    __nanosleep(i < 8 ? 20 : 100);
+  }
+  return false;
+}
+
 // ------------------------------------------------------------------ routing
-// Top-k of the router logits and softmax weights by one warp, then the
-// routing record, written to kRouteCopies lines, and the ready flag. Runs in
-// the epilogue warp of the CTA that completes the router rows.
-template <int NPL>
-__device__ void route_topk(const DecodeArgs& a, int lane, int& my_idx, float& ps, int& ntr) {
-  float v[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < a.E ? __ldcg(&a.logits[e]) : 0.0f;
-  }
-  float sum = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) sum += v[i];
-  if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 3000 + (sum != sum ? 1 : 0));
-  warp_topk<NPL>(v, a.E, a.k, lane, my_idx, ps);
-  if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 3001 + (ps != ps ? 1 : 0));
-}
-
-__device__ void route_and_publish(const DecodeArgs& a, int lane, int& ntr) {
-  int my_idx;
-  float ps;
-  if (a.E <= 256) route_topk<8>(a, lane, my_idx, ps, ntr);
-  else route_topk<kMaxEPerLane>(a, lane, my_idx, ps, ntr);
-  if (lane < a.k) {
-    if (a.dbg.idx) a.dbg.idx[lane] = my_idx;
-    if (a.dbg.p) a.dbg.p[lane] = ps;
-  }
-  // lanes 0..7 write idx, lanes 8..15 write p, into every copy
-  const float pl = __shfl_sync(0xffffffffu, ps, lane & 7);
-  const uint32_t word = lane < 8 ? static_cast<uint32_t>(my_idx) : __float_as_uint(pl);
-  if (lane < 16 && (lane & 7) < a.k)
-    for (int c = 0; c < kRouteCopies; ++c) a.ctr[a.route_base + kCtrLine * c + lane] = word;
-  __syncwarp();
-  if (lane == 0) red_add_release(&a.ctr[kCtrRouteReady], 1u);
-  if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 3002);
-}
-
 // Waits for the routing record and loads this CTA's copy (one warp).
 __device__ void fetch_route(const DecodeArgs& a, DecodeSmem& sm, int lane) {
   if (lane == 0 && !spin_until_geq(&a.ctr[kCtrRouteReady], 1u)) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
@@ -232,6 +210,69 @@ __device__ void fetch_route(const DecodeArgs& a, DecodeSmem& sm, int lane) {
     sm.p[lane] = __uint_as_float(__ldcg(rec + 8 + lane));
   }
   __syncwarp();
+}
+
+// The routing item, run by one compute group (256 threads, named barrier bar):
+// the rank of every logit among all E (key order: larger value, then lower
+// index, NaN last) selects the top k in order; the softmax weights are taken
+// over all E; the routing record goes to kRouteCopies lines, then the flag.
+__device__ void route_item(const DecodeArgs& a, DecodeSmem& sm, int bar, int t) {
+  const int warp = t >> 5, lane = t & 31;
+  if (t == 0 && !spin_until_geq(&a.ctr[kCtrRouter], static_cast<uint32_t>(a.nR)))
+    set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+  named_bar(bar, kGroupThreads);
+  float l[kMaxE / kGroupThreads];
+#pragma unroll
+  for (int j = 0; j < kMaxE / kGroupThreads; ++j) {
+    const int e = t + kGroupThreads * j;
+    l[j] = e < a.E ? __ldcg(&a.logits[e]) : 0.0f;
+    if (e < a.E) sm.rkey[e] = ranks_key(l[j], e);
+  }
+  named_bar(bar, kGroupThreads);
+#pragma unroll
+  for (int j = 0; j < kMaxE / kGroupThreads; ++j) {
+    const int e = t + kGroupThreads * j;
+    if (e < a.E) {
+      const uint64_t mine = sm.rkey[e];
+      int rank = 0;
+#pragma unroll 8
+      for (int o = 0; o < a.E; ++o) rank += sm.rkey[o] > mine ? 1 : 0;
+      if (rank < a.k) {
+        sm.idx[rank] = e;
+        sm.p[rank] = l[j];  // the logit for now
+      }
+    }
+  }
+  named_bar(bar, kGroupThreads);
+  const float m = sm.p[0];
+  float z = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kMaxE / kGroupThreads; ++j) {
+    const int e = t + kGroupThreads * j;
+    if (e < a.E && !isnan(l[j])) z += expf(l[j] - m);
+  }
+  z = warp_sum_canonical(z);
+  if (lane == 0) sm.rwarp[warp] = z;
+  named_bar(bar, kGroupThreads);
+  if (t < a.k) {
+    float zt = 0.0f;
+    for (int w = 0; w < kGroupWarps; ++w) zt += sm.rwarp[w];
+    const float ps = __fdiv_rn(expf(sm.p[t] - m), zt);
+    if (a.dbg.idx) a.dbg.idx[t] = sm.idx[t];
+    if (a.dbg.p) a.dbg.p[t] = ps;
+    sm.p[t] = ps;  // each thread reads and writes only its own entry here
+  }
+  named_bar(bar, kGroupThreads);
+  // 16 words (idx[8], p[8]) x kRouteCopies lines
+  for (int w = t; w < 16 * kRouteCopies; w += kGroupThreads) {
+    const int c = w >> 4, i = w & 15;
+    if ((i & 7) < a.k) {
+      const uint32_t word = i < 8 ? static_cast<uint32_t>(sm.idx[i]) : __float_as_uint(sm.p[i - 8]);
+      a.ctr[a.route_base + kCtrLine * c + i] = word;
+    }
+  }
+  named_bar(bar, kGroupThreads);
+  if (t == 0) red_add_release(&a.ctr[kCtrRouteReady], 1u);
 }
 
 // Codebooks of a slot's expert (gate, up, down) into shared memory.
@@ -282,6 +323,10 @@ __device__ void prefetch_down(const DecodeArgs& a, const DecodeSmem& sm, int slo
 __device__ void issue_unit(const DecodeArgs& a, DecodeSmem& sm, int s, const Unit& un) {
   uint8_t* st = sm.stage[s];
   uint64_t* bar = &sm.full[s];
+  if (un.kind == U_ROUTE) {
+    mbar_arrive(bar);  // no data
+    return;
+  }
   if (un.kind == U_ROUTER) {
     const uint32_t bytes = kRouterRows * a.H * 2;
     mbar_arrive_expect_tx(bar, bytes);
@@ -445,12 +490,36 @@ __device__ float router_row(const DecodeArgs& a, const DecodeSmem& sm, const uin
   return warp_sum_canonical(acc);
 }
 
-// Computes fill un from stage s with the 8 warps of one compute group (wg =
-// warp in group); releases the stage as soon as it is read; results go to
-// shared memory (h, for epilogue entry e) or global memory (logits, o).
-__device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int e, const Unit& un,
-                             int wg, int lane) {
+// Rotates (H32) and quantizes (Q8) one 32-block of h of slot by one warp;
+// lane i holds element i. Publishes the block.
+__device__ void quantize_h_block(const DecodeArgs& a, float v, int slot, int blk, int lane) {
+  if (a.signs_h) v = h32_warp(v, __ldg(&a.signs_h[blk]), lane);
+  uint16_t db;
+  const int8_t q = q8_warp(v, db);
+  const size_t base = static_cast<size_t>(slot) * a.I + 32 * blk;
+  a.hq[base + lane] = q;
+  if (lane == 0) reinterpret_cast<uint16_t*>(a.hd + static_cast<size_t>(slot) * a.hd_stride)[blk] = db;
+  if (a.dbg.hq) a.dbg.hq[base + lane] = q;
+  if (a.dbg.hd && lane == 0) a.dbg.hd[static_cast<size_t>(slot) * (a.I / 32) + blk] = db;
+  __syncwarp();
+  if (lane == 0) red_add_release(&a.ctr[kCtrHqDone + kCtrLine * slot], 1u);
+}
+
+// Computes fill n (unit un) from stage s with the 8 warps of compute group grp
+// (wg = warp in group), releasing the stage as soon as it is read, then does
+// the fill's share of publishing. first_prev: this group's previous first-half
+// gate/up fill (-1 if none).
+__device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int n, const Unit& un,
+                             int grp, int wg, int lane, int& first_prev) {
   const uint8_t* st = sm.stage[s];
+  const int bar = kBarGroup + grp;
+  const int t = wg * 32 + lane;
+  if (un.kind == U_ROUTE) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    route_item(a, sm, bar, t);
+    return;
+  }
   if (un.kind == U_ROUTER) {
     float l = 0.0f;
     if (wg < kRouterRows) l = router_row(a, sm, st, wg, lane);
@@ -461,6 +530,8 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int e, 
       a.logits[ex] = l;
       if (a.dbg.logits) a.dbg.logits[ex] = l;
     }
+    named_bar(bar, kGroupThreads);
+    if (t == 0) red_add_release(&a.ctr[kCtrRouter], 1u);
     return;
   }
   if (un.kind == U_SGU || un.kind == U_GU) {
@@ -477,15 +548,45 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int e, 
     else if (fmt == 3) gu_rows<3>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
     else gu_rows<4>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
     __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    const bool first_half = (un.chunk & 1) == 0;
+    if (first_half && first_prev >= 0) {
+      // the other group must have consumed this group's previous first half
+      if (t == 0 && !smem_wait_eq(&sm.hs_ack[grp], first_prev)) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+      named_bar(bar, kGroupThreads);
+    }
+    float* hs = first_half ? sm.hs_first[grp] : sm.hs_second[grp];
     if (lane == 0) {
-      mbar_arrive(&sm.empty[s]);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int r = wg + kGroupWarps * j;
         const float h = g[j] * u[j] / (1.0f + expf(-g[j]));
-        sm.hs[e][r] = h;
+        hs[r] = h;
         if (a.dbg.h) a.dbg.h[static_cast<size_t>(un.slot) * a.I + base + r] = h;
       }
+    }
+    named_bar(bar, kGroupThreads);
+    if (first_half) {
+      if (t == 0) {
+        __threadfence_block();
+        sm.hs_seq[grp] = n;
+      }
+      first_prev = n;
+      return;
+    }
+    // second half: the first half was fill n - 1, computed by the other group
+    if (wg == 0) {
+      const int other = grp ^ 1;
+      if (lane == 0 && !smem_wait_eq(&sm.hs_seq[other], n - 1)) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+      __syncwarp();
+      __threadfence_block();
+      const float v = lane < kGuRows ? sm.hs_first[other][lane] : sm.hs_second[grp][lane - kGuRows];
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        sm.hs_ack[other] = n - 1;
+      }
+      quantize_h_block(a, v, un.slot, un.chunk / 2, lane);
     }
     return;
   }
@@ -508,23 +609,8 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int e, 
       if (a.dbg.o) a.dbg.o[at] = o[j];
     }
   }
-}
-
-// ------------------------------------------------------------------ epilogue side
-// Quantizes one 32-block of h whose halves sit in epilogue entries e0, e1.
-__device__ void quantize_h_block(const DecodeArgs& a, const DecodeSmem& sm, int e0, int e1,
-                                 int slot, int blk, int lane) {
-  float v = lane < kGuRows ? sm.hs[e0][lane] : sm.hs[e1][lane - kGuRows];
-  if (a.signs_h) v = h32_warp(v, __ldg(&a.signs_h[blk]), lane);
-  uint16_t db;
-  const int8_t q = q8_warp(v, db);
-  const size_t base = static_cast<size_t>(slot) * a.I + 32 * blk;
-  a.hq[base + lane] = q;
-  if (lane == 0) reinterpret_cast<uint16_t*>(a.hd + static_cast<size_t>(slot) * a.hd_stride)[blk] = db;
-  if (a.dbg.hq) a.dbg.hq[base + lane] = q;
-  if (a.dbg.hd && lane == 0) a.dbg.hd[static_cast<size_t>(slot) * (a.I / 32) + blk] = db;
-  __syncwarp();
-  if (lane == 0) red_add_release(&a.ctr[kCtrHqDone + kCtrLine * slot], 1u);
+  named_bar(bar, kGroupThreads);
+  if (t == 0) red_add_release(&a.ctr[kCtrDownDone], 1u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
@@ -537,13 +623,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kGroupWarps);
     }
-    for (int e = 0; e < kEpi; ++e) {
-      mbar_init(&sm.epi_full[e], kGroupWarps);
-      mbar_init(&sm.epi_empty[e], 1);
-    }
     sm.issued = 0;
     sm.have_route = 0;
-    for (int g = 0; g < kGroups; ++g) sm.consumed[g] = g - kGroups;
+    for (int g = 0; g < kGroups; ++g) {
+      sm.consumed[g] = g - kGroups;
+      sm.hs_seq[g] = -1;
+      sm.hs_ack[g] = -1;
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -607,46 +693,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       if (aborted || nf == 0) break;
     }
     if (lane == 0) sm.issued = it;
-  } else if (warp == kEpilogueWarp) {
-    // ---------------------------------------------------------------- epilogue warp
-    int ntr = 0;
-    for (int n = 0;; ++n) {
-      const int e = n % kEpi;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&sm.epi_full[e], (n / kEpi) & 1);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-        set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
-        break;
-      }
-      const Unit un = unpack_unit(sm.epi_unit[e]);
-      if (un.kind == U_END) break;
-      if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_EPI_BEGIN, pack_unit(un));
-      bool release = true;
-      if (un.kind == U_ROUTER) {
-        uint32_t old = 0;
-        if (lane == 0) old = atom_add_acq_rel(&a.ctr[kCtrRouter], 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        __syncwarp();
-        if (lane == 0) trace_ev(a, 2, ntr, MOEQ_TRACE_SPIN, 2999);
-        if (old == static_cast<uint32_t>(a.nR - 1)) route_and_publish(a, lane, ntr);
-      } else if (un.kind == U_SGU || un.kind == U_GU) {
-        if ((un.chunk & 1) == 0) {
-          release = false;  // first half: its h waits in sm.hs[e] for the second half
-        } else {
-          const int ep = (n + kEpi - 1) % kEpi;
-          quantize_h_block(a, sm, ep, e, un.slot, un.chunk / 2, lane);
-          if (lane == 0) mbar_arrive(&sm.epi_empty[ep]);
-        }
-      } else {
-        __syncwarp();
-        if (lane == 0) red_add_release(&a.ctr[kCtrDownDone], 1u);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        if (release) mbar_arrive(&sm.epi_empty[e]);
-        trace_ev(a, 2, ntr, MOEQ_TRACE_EPI_END, pack_unit(un));
-      }
-    }
   } else {
     // ---------------------------------------------------------------- compute warps
     const int nbH = a.H / 32;
@@ -674,17 +720,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     named_bar(kBarCompute, kComputeThreads);
     const int grp = warp / kGroupWarps, wg = warp % kGroupWarps;
     const int role = grp == 0 ? 0 : 3;
-    int ntr = 0;
+    int ntr = 0, first_prev = -1;
     if (wg == 0 && lane == 0) trace_ev(a, role, ntr, MOEQ_TRACE_START, 0);
 
     for (int it = grp;; it += kGroups) {
       const int s = it % kStages;
-      const int e = it % kEpi;
       bool ok = true;
-      if (lane == 0) {
-        ok = mbar_wait(&sm.full[s], (it / kStages) & 1);
-        if (ok && it >= kEpi) ok = mbar_wait(&sm.epi_empty[e], ((it / kEpi) - 1) & 1);
-      }
+      if (lane == 0) ok = mbar_wait(&sm.full[s], (it / kStages) & 1);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
         set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
         break;
@@ -695,14 +737,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
         trace_ev(a, role, ntr, MOEQ_TRACE_READY, u);
       }
       const Unit un = unpack_unit(u);
-      if (un.kind != U_END) compute_unit(a, sm, s, e, un, wg, lane);
-      if (wg == 0 && lane == 0) {
-        trace_ev(a, role, ntr, MOEQ_TRACE_DONE, u);
-        sm.epi_unit[e] = u;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.epi_full[e]);
       if (un.kind == U_END) break;
+      compute_unit(a, sm, s, it, un, grp, wg, lane, first_prev);
+      if (wg == 0 && lane == 0) trace_ev(a, role, ntr, MOEQ_TRACE_DONE, u);
     }
   }
 
@@ -808,10 +845,10 @@ extern "C" int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, 
   if (dbg) a.dbg = *dbg;
   a.nR = L->E / kRouterRows;
   a.nSG = a.has_shared ? L->I / (2 * kGuRows) : 0;
-  a.nGU = L->k * (L->I / (2 * kGuRows));
   a.nSD = a.has_shared ? L->H / kDownRows : 0;
+  a.nGU = L->k * (L->I / (2 * kGuRows));
   a.nD = L->k * (L->H / kDownRows);
-  a.items = a.nR + a.nSG + a.nGU + a.nSD + a.nD;
+  a.items = a.nR + a.nSG + 1 + a.nSD + a.nGU + a.nD;
   a.route_base = route_base(a.nslots);
   a.n_ctr = static_cast<int>(wl.n_ctr);
 
