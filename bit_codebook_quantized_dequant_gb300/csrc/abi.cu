@@ -27,7 +27,7 @@ int validate_matrix(const moeq_matrix& m, int rows, int cols, int experts) {
   if (m.cb_len < need) return MOEQ_ERR_CODEBOOK_TRUNCATED;
   if (m.cb_len > need) return MOEQ_ERR_CODEBOOK_MISMATCH;
   if (experts > 1 && m.cb_stride < m.cb_len) return MOEQ_ERR_CODEBOOK_DUPLICATE;
-  if ((reinterpret_cast<uintptr_t>(m.codebooks) & 3u) || (m.cb_stride & 3)) return MOEQ_ERR_ALIGN;
+  if (!aligned16(m.codebooks) || (experts > 1 && m.cb_stride % 16)) return MOEQ_ERR_ALIGN;
   return MOEQ_OK;
 }
 

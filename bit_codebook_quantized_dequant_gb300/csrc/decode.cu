@@ -5,9 +5,12 @@
 //   router rows (4 per item)
 //   -> shared-expert gate/up (32 rows per item, as two 16-row fills)
 //   -> routing (one item: top-k and softmax weights of the router logits)
-//   -> shared-expert down rows (32 per item)
 //   -> routed gate/up (32 rows per item, slot-major)
+//   -> shared-expert down rows (32 per item)
 //   -> routed down rows (32 per item, slot-major)
+// (item_fills can also place a slot's down rows a fixed number of slots after
+// its gate/up rows; measured slower, since a producer that waits for one slot's
+// h holds back the fills queued behind it.)
 //   -> (after every down item) the combine of y.
 // An item only waits on items with a smaller queue index, and every CTA is
 // resident (cooperative launch), so every wait ends; each is bounded anyway and
@@ -61,10 +64,10 @@ constexpr int kRouterRows = 4;
 constexpr int kGuRows = 16;  // rows per gate/up fill; an item is two fills (one 32-block of h)
 constexpr int kDownRows = 32;
 constexpr int kMaxH = 4096;
-constexpr int kMaxB = kMaxH / 32 / 32;  // 32-blocks per lane along K
 constexpr int kMaxE = 512;
 constexpr int kBarCompute = 1;  // named barrier of all compute warps
 constexpr int kBarGroup = 2;    // named barriers 2, 3: one per compute group
+constexpr int kDownLag = kMaxK;  // slots between a slot's gate/up items and its down items
 
 enum UnitKind { U_ROUTER = 0, U_SGU, U_GU, U_SDOWN, U_DOWN, U_ROUTE, U_END };
 
@@ -107,13 +110,13 @@ struct alignas(128) DecodeSmem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int unit[kStages];
-  uint64_t rkey[kMaxE];             // routing item: ranking keys
+  uint64_t rkey[kGroupWarps * kMaxK];  // routing item: per-warp candidate keys
+  uint32_t stage_cb[kStages][8];       // codebook records of the fill in each stage
   float rwarp[kGroupWarps];         // routing item: per-warp softmax partial sums
   float hs_first[kGroups][kGuRows];   // h of a first-half gate/up fill, by group
   float hs_second[kGroups][kGuRows];  // h of a second-half gate/up fill, by group
   volatile int hs_seq[kGroups];       // fill index of the first half in hs_first[g]
   volatile int hs_ack[kGroups];       // fill index of the first half last consumed from it
-  uint32_t slot_cb[kMaxK + 1][12];  // codebooks of each slot's expert: gate, up, down
   int idx[kMaxK];
   float p[kMaxK];
   int have_route;
@@ -131,13 +134,25 @@ __device__ __forceinline__ int item_fills(const DecodeArgs& a, int i, Unit& firs
   i -= a.nSG;
   if (i == 0) { first = Unit{U_ROUTE, 0, 0}; return 1; }
   i -= 1;
+  // routed work, with the down rows of slot s placed after the gate/up rows of
+  // slot s + kDownLag so that a slot's h is complete before its down items come:
+  //   GU(0) .. GU(lag-1), then for s >= lag: GU(s) D(s-lag), then SD, D(k-lag) ..
+  const int pairs = a.I / (2 * kGuRows);
+  const int per = a.H / kDownRows;
+  const int lag = a.k < kDownLag ? a.k : kDownLag;
+  if (i < lag * pairs) { first = Unit{U_GU, i / pairs, 2 * (i % pairs)}; return 2; }
+  i -= lag * pairs;
+  const int round = pairs + per;
+  if (i < (a.k - lag) * round) {
+    const int s = lag + i / round, j = i % round;
+    if (j < pairs) { first = Unit{U_GU, s, 2 * j}; return 2; }
+    first = Unit{U_DOWN, s - lag, j - pairs};
+    return 1;
+  }
+  i -= (a.k - lag) * round;
   if (i < a.nSD) { first = Unit{U_SDOWN, a.k, i}; return 1; }
   i -= a.nSD;
-  const int pairs = a.I / (2 * kGuRows);
-  if (i < a.nGU) { first = Unit{U_GU, i / pairs, 2 * (i % pairs)}; return 2; }
-  i -= a.nGU;
-  const int per = a.H / kDownRows;
-  first = Unit{U_DOWN, i / per, i % per};
+  first = Unit{U_DOWN, a.k - lag + i / per, i % per};
   return 1;
 }
 
@@ -200,11 +215,11 @@ __device__ __forceinline__ bool smem_wait_eq(const volatile int* w, int want) {
 }
 
 // ------------------------------------------------------------------ routing
-// Waits for the routing record and loads this CTA's copy (one warp).
+// Waits for this CTA's copy of the routing record and loads it (one warp).
 __device__ void fetch_route(const DecodeArgs& a, DecodeSmem& sm, int lane) {
-  if (lane == 0 && !spin_until_geq(&a.ctr[kCtrRouteReady], 1u)) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
-  __syncwarp();
   const uint32_t* rec = a.ctr + a.route_base + kCtrLine * (blockIdx.x % kRouteCopies);
+  if (lane == 0 && !spin_until_geq(rec + kRouteFlag, 1u)) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+  __syncwarp();
   if (lane < a.k) {
     sm.idx[lane] = static_cast<int>(__ldcg(rec + lane));
     sm.p[lane] = __uint_as_float(__ldcg(rec + 8 + lane));
@@ -213,42 +228,46 @@ __device__ void fetch_route(const DecodeArgs& a, DecodeSmem& sm, int lane) {
 }
 
 // The routing item, run by one compute group (256 threads, named barrier bar):
-// the rank of every logit among all E (key order: larger value, then lower
-// index, NaN last) selects the top k in order; the softmax weights are taken
-// over all E; the routing record goes to kRouteCopies lines, then the flag.
+// every warp selects the top k of its logits, one warp selects the top k of
+// those candidates (key order: larger value, then lower index, NaN last), the
+// softmax weights are taken over all E, and the routing record goes to
+// kRouteCopies lines, each published by its own release store.
 __device__ void route_item(const DecodeArgs& a, DecodeSmem& sm, int bar, int t) {
+  constexpr int NPL = kMaxE / kGroupThreads;  // logits per thread
   const int warp = t >> 5, lane = t & 31;
   if (t == 0 && !spin_until_geq(&a.ctr[kCtrRouter], static_cast<uint32_t>(a.nR)))
     set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
   named_bar(bar, kGroupThreads);
-  float l[kMaxE / kGroupThreads];
+  float l[NPL];
+  uint64_t key[NPL];
 #pragma unroll
-  for (int j = 0; j < kMaxE / kGroupThreads; ++j) {
-    const int e = t + kGroupThreads * j;
+  for (int j = 0; j < NPL; ++j) {
+    const int e = warp * 32 * NPL + 32 * j + lane;  // a warp owns a contiguous range
     l[j] = e < a.E ? __ldcg(&a.logits[e]) : 0.0f;
-    if (e < a.E) sm.rkey[e] = ranks_key(l[j], e);
+    key[j] = e < a.E ? ranks_key(l[j], e) : 0ull;
   }
+  const uint64_t cand = warp_select_keys<NPL>(key, a.k, lane);
+  if (lane < a.k) sm.rkey[warp * kMaxK + lane] = cand;
   named_bar(bar, kGroupThreads);
+  if (warp == 0) {
+    uint64_t k2[2];
 #pragma unroll
-  for (int j = 0; j < kMaxE / kGroupThreads; ++j) {
-    const int e = t + kGroupThreads * j;
-    if (e < a.E) {
-      const uint64_t mine = sm.rkey[e];
-      int rank = 0;
-#pragma unroll 8
-      for (int o = 0; o < a.E; ++o) rank += sm.rkey[o] > mine ? 1 : 0;
-      if (rank < a.k) {
-        sm.idx[rank] = e;
-        sm.p[rank] = l[j];  // the logit for now
-      }
+    for (int j = 0; j < 2; ++j) {
+      const int c = lane + 32 * j;  // candidates: kGroupWarps x kMaxK = 64
+      k2[j] = (c % kMaxK) < a.k ? sm.rkey[c] : 0ull;
+    }
+    const uint64_t top = warp_select_keys<2>(k2, a.k, lane);
+    if (lane < a.k) {
+      sm.idx[lane] = key_index(top);
+      sm.p[lane] = key_value(top);  // the logit for now
     }
   }
   named_bar(bar, kGroupThreads);
   const float m = sm.p[0];
   float z = 0.0f;
 #pragma unroll
-  for (int j = 0; j < kMaxE / kGroupThreads; ++j) {
-    const int e = t + kGroupThreads * j;
+  for (int j = 0; j < NPL; ++j) {
+    const int e = warp * 32 * NPL + 32 * j + lane;
     if (e < a.E && !isnan(l[j])) z += expf(l[j] - m);
   }
   z = warp_sum_canonical(z);
@@ -263,32 +282,19 @@ __device__ void route_item(const DecodeArgs& a, DecodeSmem& sm, int bar, int t) 
     sm.p[t] = ps;  // each thread reads and writes only its own entry here
   }
   named_bar(bar, kGroupThreads);
-  // 16 words (idx[8], p[8]) x kRouteCopies lines
-  for (int w = t; w < 16 * kRouteCopies; w += kGroupThreads) {
-    const int c = w >> 4, i = w & 15;
-    if ((i & 7) < a.k) {
-      const uint32_t word = i < 8 ? static_cast<uint32_t>(sm.idx[i]) : __float_as_uint(sm.p[i - 8]);
-      a.ctr[a.route_base + kCtrLine * c + i] = word;
-    }
-  }
-  named_bar(bar, kGroupThreads);
-  if (t == 0) red_add_release(&a.ctr[kCtrRouteReady], 1u);
-}
-
-// Codebooks of a slot's expert (gate, up, down) into shared memory.
-__device__ __forceinline__ void load_cb_words(const DMat& m, int e, uint32_t* w) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(m.cb + static_cast<size_t>(e) * m.cb_stride);
-  const int n = (1 << m.fmt) / 4;
+  if (t < kRouteCopies) {
+    uint32_t* rec = a.ctr + a.route_base + kCtrLine * t;
+    uint32_t w[16];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) w[i] = i < n ? __ldg(p + i) : 0u;
-}
-
-__device__ void stage_slot_cb(const DecodeArgs& a, DecodeSmem& sm, int slot) {
-  const bool shared = slot == a.k;
-  const int e = shared ? 0 : sm.idx[slot];
-  load_cb_words(shared ? a.sgate : a.gate, e, sm.slot_cb[slot]);
-  load_cb_words(shared ? a.sup : a.up, e, sm.slot_cb[slot] + 4);
-  load_cb_words(shared ? a.sdown : a.down, e, sm.slot_cb[slot] + 8);
+    for (int i = 0; i < 8; ++i) {
+      w[i] = i < a.k ? static_cast<uint32_t>(sm.idx[i]) : 0u;
+      w[8 + i] = i < a.k ? __float_as_uint(sm.p[i]) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      reinterpret_cast<uint4*>(rec)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    st_release(rec + kRouteFlag, 1u);
+  }
 }
 
 // ------------------------------------------------------------------ producer side
@@ -343,11 +349,13 @@ __device__ void issue_unit(const DecodeArgs& a, DecodeSmem& sm, int s, const Uni
     const size_t r0 = static_cast<size_t>(un.chunk) * kGuRows;
     const uint32_t cbytes = static_cast<uint32_t>(kGuRows * pc);
     const uint32_t sbytes = static_cast<uint32_t>(kGuRows * ps);
-    mbar_arrive_expect_tx(bar, 2 * (cbytes + sbytes));
+    mbar_arrive_expect_tx(bar, 2 * (cbytes + sbytes) + 32);
     bulk_g2s(st + mp.ca, G.codes + e * G.stride_codes + r0 * pc, cbytes, bar);
     bulk_g2s(st + mp.sa, G.scales + e * G.stride_scales + r0 * ps, sbytes, bar);
     bulk_g2s(st + mp.cb, U.codes + e * U.stride_codes + r0 * pc, cbytes, bar);
     bulk_g2s(st + mp.sb, U.scales + e * U.stride_scales + r0 * ps, sbytes, bar);
+    bulk_g2s(sm.stage_cb[s], G.cb + static_cast<size_t>(e) * G.cb_stride, 16, bar);
+    bulk_g2s(sm.stage_cb[s] + 4, U.cb + static_cast<size_t>(e) * U.cb_stride, 16, bar);
     return;
   }
   // down fill: weights now, this slot's quantized h once it is complete
@@ -357,9 +365,11 @@ __device__ void issue_unit(const DecodeArgs& a, DecodeSmem& sm, int s, const Uni
   uint32_t cbytes, sbytes;
   down_src(a, sm, un.slot, un.chunk, c, cbytes, sc, sbytes);
   const uint32_t hqb = static_cast<uint32_t>(a.I), hdb = static_cast<uint32_t>(a.hd_stride);
-  mbar_arrive_expect_tx(bar, cbytes + sbytes + hqb + hdb);
+  mbar_arrive_expect_tx(bar, cbytes + sbytes + hqb + hdb + 16);
   bulk_g2s(st + mp.ca, c, cbytes, bar);
   bulk_g2s(st + mp.sa, sc, sbytes, bar);
+  const int e = un.kind == U_SDOWN ? 0 : sm.idx[un.slot];
+  bulk_g2s(sm.stage_cb[s], D.cb + static_cast<size_t>(e) * D.cb_stride, 16, bar);
   if (!spin_until_geq(&a.ctr[kCtrHqDone + kCtrLine * un.slot], static_cast<uint32_t>(a.I / 32)))
     set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -377,7 +387,7 @@ __device__ __forceinline__ void load_q(const int8_t* p, int* q) {
 
 // Rows r0 and r1 of the gate and up tiles in the stage against the quantized x
 // in shared memory: g[0], u[0] for r0 and g[1], u[1] for r1.
-template <int FMT>
+template <int FMT, bool DBG>
 __device__ void gu_rows(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t* st,
                         const uint32_t* cbg, const uint32_t* cbu, int r0, int r1, int row_base,
                         int slot, int lane, float* g, float* u) {
@@ -394,10 +404,9 @@ __device__ void gu_rows(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t
   const uint8_t* us0 = st + mp.sb + r0 * nb * SB;
   const uint8_t* us1 = st + mp.sb + r1 * nb * SB;
   float ag0 = 0.0f, au0 = 0.0f, ag1 = 0.0f, au1 = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kMaxB; ++i) {
-    const int b = lane + 32 * i;
-    if (b < nb) {
+#pragma unroll 1
+  for (int b = lane; b < nb; b += 32) {
+    {
       int q[8];
       load_q(sm.xq + 32 * b, q);
       const float xd = sm.xd[b];
@@ -409,11 +418,11 @@ __device__ void gu_rows(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t
       au0 = fmaf(block_scale<FMT>(us0, b) * xd, static_cast<float>(su0), au0);
       ag1 = fmaf(block_scale<FMT>(gs1, b) * xd, static_cast<float>(sg1), ag1);
       au1 = fmaf(block_scale<FMT>(us1, b) * xd, static_cast<float>(su1), au1);
-      if (a.dbg.S_gate) {
+      if (DBG && a.dbg.S_gate) {
         a.dbg.S_gate[(static_cast<size_t>(slot) * a.I + row_base + r0) * nb + b] = sg0;
         a.dbg.S_gate[(static_cast<size_t>(slot) * a.I + row_base + r1) * nb + b] = sg1;
       }
-      if (a.dbg.S_up) {
+      if (DBG && a.dbg.S_up) {
         a.dbg.S_up[(static_cast<size_t>(slot) * a.I + row_base + r0) * nb + b] = su0;
         a.dbg.S_up[(static_cast<size_t>(slot) * a.I + row_base + r1) * nb + b] = su1;
       }
@@ -431,7 +440,7 @@ __device__ void gu_rows(const DecodeArgs& a, const DecodeSmem& sm, const uint8_t
 
 // Rows wg, wg + 8, wg + 16, wg + 24 of the down tile in the stage against the
 // slot's quantized h, which the producer placed in the same stage.
-template <int FMT>
+template <int FMT, bool DBG>
 __device__ void down_rows(const DecodeArgs& a, const uint8_t* st, const uint32_t* cb, int wg,
                           int lane, int chunk, int slot, float* o) {
   constexpr int BC = block_bytes<FMT>();
@@ -444,10 +453,9 @@ __device__ void down_rows(const DecodeArgs& a, const uint8_t* st, const uint32_t
   float acc[R];
 #pragma unroll
   for (int j = 0; j < R; ++j) acc[j] = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kMaxB; ++i) {
-    const int b = lane + 32 * i;
-    if (b < nb) {
+#pragma unroll 1
+  for (int b = lane; b < nb; b += 32) {
+    {
       int q[8];
       load_q(hq + 32 * b, q);
       const float hdf = f16_bits_to_f32(hd[b]);
@@ -456,7 +464,7 @@ __device__ void down_rows(const DecodeArgs& a, const uint8_t* st, const uint32_t
         const int r = wg + kGroupWarps * j;
         const int d = block_dot<FMT>(st + mp.ca + r * nb * BC + b * BC, cb, q);
         acc[j] = fmaf(block_scale<FMT>(st + mp.sa + r * nb * SB, b) * hdf, static_cast<float>(d), acc[j]);
-        if (a.dbg.S_down)
+        if (DBG && a.dbg.S_down)
           a.dbg.S_down[(static_cast<size_t>(slot) * a.H + chunk * kDownRows + r) * nb + b] = d;
       }
     }
@@ -509,6 +517,7 @@ __device__ void quantize_h_block(const DecodeArgs& a, float v, int slot, int blk
 // (wg = warp in group), releasing the stage as soon as it is read, then does
 // the fill's share of publishing. first_prev: this group's previous first-half
 // gate/up fill (-1 if none).
+template <bool DBG>
 __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int n, const Unit& un,
                              int grp, int wg, int lane, int& first_prev) {
   const uint8_t* st = sm.stage[s];
@@ -528,7 +537,7 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int n, 
     if (wg < kRouterRows && lane == 0) {
       const int ex = un.chunk * kRouterRows + wg;
       a.logits[ex] = l;
-      if (a.dbg.logits) a.dbg.logits[ex] = l;
+      if (DBG && a.dbg.logits) a.dbg.logits[ex] = l;
     }
     named_bar(bar, kGroupThreads);
     if (t == 0) red_add_release(&a.ctr[kCtrRouter], 1u);
@@ -539,14 +548,14 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int n, 
     uint32_t cbg[4], cbu[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      cbg[i] = sm.slot_cb[un.slot][i];
-      cbu[i] = sm.slot_cb[un.slot][4 + i];
+      cbg[i] = sm.stage_cb[s][i];
+      cbu[i] = sm.stage_cb[s][4 + i];
     }
     const int base = un.chunk * kGuRows;
     float g[2], u[2];
-    if (fmt == 2) gu_rows<2>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
-    else if (fmt == 3) gu_rows<3>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
-    else gu_rows<4>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
+    if (fmt == 2) gu_rows<2, DBG>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
+    else if (fmt == 3) gu_rows<3, DBG>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
+    else gu_rows<4, DBG>(a, sm, st, cbg, cbu, wg, wg + kGroupWarps, base, un.slot, lane, g, u);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
     const bool first_half = (un.chunk & 1) == 0;
@@ -562,7 +571,7 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int n, 
         const int r = wg + kGroupWarps * j;
         const float h = g[j] * u[j] / (1.0f + expf(-g[j]));
         hs[r] = h;
-        if (a.dbg.h) a.dbg.h[static_cast<size_t>(un.slot) * a.I + base + r] = h;
+        if (DBG && a.dbg.h) a.dbg.h[static_cast<size_t>(un.slot) * a.I + base + r] = h;
       }
     }
     named_bar(bar, kGroupThreads);
@@ -593,12 +602,12 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int n, 
   const int fmt = un.kind == U_SDOWN ? a.sdown.fmt : a.down.fmt;
   uint32_t cb[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) cb[i] = sm.slot_cb[un.slot][8 + i];
+  for (int i = 0; i < 4; ++i) cb[i] = sm.stage_cb[s][i];
   constexpr int R = kDownRows / kGroupWarps;
   float o[R];
-  if (fmt == 2) down_rows<2>(a, st, cb, wg, lane, un.chunk, un.slot, o);
-  else if (fmt == 3) down_rows<3>(a, st, cb, wg, lane, un.chunk, un.slot, o);
-  else down_rows<4>(a, st, cb, wg, lane, un.chunk, un.slot, o);
+  if (fmt == 2) down_rows<2, DBG>(a, st, cb, wg, lane, un.chunk, un.slot, o);
+  else if (fmt == 3) down_rows<3, DBG>(a, st, cb, wg, lane, un.chunk, un.slot, o);
+  else down_rows<4, DBG>(a, st, cb, wg, lane, un.chunk, un.slot, o);
   __syncwarp();
   if (lane == 0) {
     mbar_arrive(&sm.empty[s]);
@@ -606,13 +615,14 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem& sm, int s, int n, 
     for (int j = 0; j < R; ++j) {
       const size_t at = static_cast<size_t>(un.slot) * a.H + un.chunk * kDownRows + wg + kGroupWarps * j;
       a.obuf[at] = o[j];
-      if (a.dbg.o) a.dbg.o[at] = o[j];
+      if (DBG && a.dbg.o) a.dbg.o[at] = o[j];
     }
   }
   named_bar(bar, kGroupThreads);
   if (t == 0) red_add_release(&a.ctr[kCtrDownDone], 1u);
 }
 
+template <bool DBG>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
@@ -636,10 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer warp
-    if (lane == 0 && a.has_shared) {
-      stage_slot_cb(a, sm, a.k);
-      prefetch_down(a, sm, a.k, a.k + 1);
-    }
+    if (lane == 0 && a.has_shared) prefetch_down(a, sm, a.k, a.k + 1);
     __syncwarp();
     int it = 0, ntr = 0;
     bool aborted = false;
@@ -654,12 +661,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       const int nf = item_fills(a, item, first);
       if (nf > 0 && (first.kind == U_GU || first.kind == U_DOWN) && !sm.have_route) {
         fetch_route(a, sm, lane);
-        if (lane < a.k) stage_slot_cb(a, sm, lane);
-        __syncwarp();
         if (lane == 0) {
           sm.have_route = 1;
           trace_ev(a, 1, ntr, MOEQ_TRACE_TOPK, item);
-          prefetch_down(a, sm, 0, a.k);
         }
         __syncwarp();
       }
@@ -738,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       }
       const Unit un = unpack_unit(u);
       if (un.kind == U_END) break;
-      compute_unit(a, sm, s, it, un, grp, wg, lane, first_prev);
+      compute_unit<DBG>(a, sm, s, it, un, grp, wg, lane, first_prev);
       if (wg == 0 && lane == 0) trace_ev(a, role, ntr, MOEQ_TRACE_DONE, u);
     }
   }
@@ -855,9 +859,14 @@ extern "C" int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, 
   const DeviceInfo& di = device_info();
   const size_t smem = sizeof(DecodeSmem);
   if (smem > di.max_smem_optin) return MOEQ_ERR_CUDA;
+  // the debug instantiation carries the stores of intermediates and the timeline
+  const bool want_dbg = dbg != nullptr;
+  void (*kern)(const DecodeArgs) = want_dbg ? decode_kernel<true> : decode_kernel<false>;
   static thread_local int configured_dev = -1;
   if (configured_dev != di.device) {
-    if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MOEQ_ERR_CUDA;
     configured_dev = di.device;
@@ -872,5 +881,5 @@ extern "C" int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, decode_kernel, a));
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, a));
 }

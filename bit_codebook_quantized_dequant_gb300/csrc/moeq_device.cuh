@@ -104,6 +104,11 @@ __device__ __forceinline__ bool spin_until_geq(const uint32_t* p, uint32_t targe
   return false;
 }
 
+// Store with release semantics at GPU scope.
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Atomic add with acquire-release semantics at GPU scope; returns the old value.
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   uint32_t old;
@@ -372,20 +377,11 @@ __device__ __forceinline__ uint64_t ranks_key(float v, int index) {
   return (static_cast<uint64_t>(ordered_bits(v)) << 32) | (0xffffffffu - static_cast<uint32_t>(index));
 }
 
-// Top-k of E values held NPL per lane (lane l holds elements l + 32 i in v[i])
-// and their softmax weights over all E: after the call lane s < k holds the
-// s-th selected index in idx and its weight exp(l_s - max) / sum exp(l - max)
-// in p. Each lane sorts its keys with a bitonic network; k rounds of a warp
-// maximum over the lanes' heads then pick the winners in order.
+// k rounds of a warp maximum over per-lane key lists: key[] of each lane is
+// sorted in place (bitonic network, descending) and after the call lane s < k
+// holds the s-th largest key of the warp (0 if fewer than s+1 keys exist).
 template <int NPL>
-__device__ __forceinline__ void warp_topk(const float (&v)[NPL], int E, int k, int lane, int& idx,
-                                          float& p) {
-  uint64_t key[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = e < E ? ranks_key(v[i], e) : 0ull;
-  }
+__device__ __forceinline__ uint64_t warp_select_keys(uint64_t (&key)[NPL], int k, int lane) {
 #pragma unroll
   for (int k2 = 2; k2 <= NPL; k2 <<= 1) {
 #pragma unroll
@@ -403,7 +399,7 @@ __device__ __forceinline__ void warp_topk(const float (&v)[NPL], int E, int k, i
       }
     }
   }
-  uint64_t mine = 0ull, first = 0ull;
+  uint64_t mine = 0ull;
   for (int s = 0; s < k; ++s) {
     uint64_t h = key[0];
 #pragma unroll
@@ -411,15 +407,38 @@ __device__ __forceinline__ void warp_topk(const float (&v)[NPL], int E, int k, i
       const uint64_t o = __shfl_xor_sync(0xffffffffu, h, d);
       h = o > h ? o : h;
     }
-    if (s == 0) first = h;
     if (lane == s) mine = h;
-    if (key[0] == h) {  // the lane that held the winner moves to its next key
+    if (h != 0ull && key[0] == h) {  // the lane that held the winner moves to its next key
 #pragma unroll
       for (int i = 0; i + 1 < NPL; ++i) key[i] = key[i + 1];
       key[NPL - 1] = 0ull;
     }
   }
-  const float m = from_ordered_bits(static_cast<uint32_t>(first >> 32));
+  return mine;
+}
+
+__device__ __forceinline__ int key_index(uint64_t key) {
+  return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+  return from_ordered_bits(static_cast<uint32_t>(key >> 32));
+}
+
+// Top-k of E values held NPL per lane (lane l holds elements l + 32 i in v[i])
+// and their softmax weights over all E: after the call lane s < k holds the
+// s-th selected index in idx and its weight exp(l_s - max) / sum exp(l - max)
+// in p.
+template <int NPL>
+__device__ __forceinline__ void warp_topk(const float (&v)[NPL], int E, int k, int lane, int& idx,
+                                          float& p) {
+  uint64_t key[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? ranks_key(v[i], e) : 0ull;
+  }
+  const uint64_t mine = warp_select_keys<NPL>(key, k, lane);
+  const float m = key_value(__shfl_sync(0xffffffffu, mine, 0));
   float z = 0.0f;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
@@ -427,8 +446,8 @@ __device__ __forceinline__ void warp_topk(const float (&v)[NPL], int E, int k, i
     if (e < E && !isnan(v[i])) z += expf(v[i] - m);
   }
   z = warp_sum_canonical(z);
-  idx = static_cast<int>(0xffffffffu - static_cast<uint32_t>(mine));
-  p = __fdiv_rn(expf(from_ordered_bits(static_cast<uint32_t>(mine >> 32)) - m), z);
+  idx = key_index(mine);
+  p = __fdiv_rn(expf(key_value(mine) - m), z);
 }
 
 }  // namespace moeq

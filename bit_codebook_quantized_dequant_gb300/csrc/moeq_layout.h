@@ -14,20 +14,20 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // many CTAs poll or update has its own 128-byte line:
 //   kCtrQueue      work queue (items taken)
 //   kCtrRouter     router items done
-//   kCtrRouteReady 1 once the routing record is published
 //   kCtrDownDone   down units done
 //   kCtrDone       CTAs finished (the last one resets the counters)
 //   kCtrHqDone + kCtrLine * s   quantized 32-blocks of h of slot s
-// followed by kRouteCopies lines holding copies of the routing record
-// (idx[8] then p[8] as fp32 bits), each read by a few CTAs only.
+// followed by kRouteCopies copies of the routing record, one line each, every
+// copy read by a few CTAs only: idx[8], p[8] (fp32 bits), and a ready flag in
+// the last word, stored with release semantics after the rest of the line.
 constexpr int kCtrLine = 32;  // words per 128-byte line
 constexpr int kCtrQueue = 0;
 constexpr int kCtrRouter = 1 * kCtrLine;
-constexpr int kCtrRouteReady = 2 * kCtrLine;
-constexpr int kCtrDownDone = 3 * kCtrLine;
-constexpr int kCtrDone = 4 * kCtrLine;
-constexpr int kCtrHqDone = 5 * kCtrLine;
-constexpr int kRouteCopies = 32;
+constexpr int kCtrDownDone = 2 * kCtrLine;
+constexpr int kCtrDone = 3 * kCtrLine;
+constexpr int kCtrHqDone = 4 * kCtrLine;
+constexpr int kRouteCopies = 16;
+constexpr int kRouteFlag = kCtrLine - 1;
 inline constexpr int route_base(int max_slots) { return kCtrHqDone + kCtrLine * max_slots; }
 inline constexpr int ctr_words(int max_slots) { return route_base(max_slots) + kCtrLine * kRouteCopies; }
 

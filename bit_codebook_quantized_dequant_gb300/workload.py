@@ -15,6 +15,9 @@ from . import (MoeqDebug, MoeqLayer, MoeqMatrix, moe_ffn_workspace, moe_ffn_work
 from . import synth as S
 
 
+CB_STRIDE = 16  # bytes per codebook record (the library reads whole 16-byte records)
+
+
 def _round(n: int, a: int = 256) -> int:
     return (n + a - 1) // a * a
 
@@ -42,7 +45,7 @@ class DeviceMatrix:
     def desc(self) -> MoeqMatrix:
         return MoeqMatrix(self.fmt, self.rows, self.cols, self.E, self.codes.data_ptr(),
                           self.stride_codes, self.scales.data_ptr(), self.stride_scales,
-                          self.codebooks.data_ptr(), 1 << self.fmt, 1 << self.fmt)
+                          self.codebooks.data_ptr(), 1 << self.fmt, CB_STRIDE)
 
     @property
     def nbytes(self) -> int:
@@ -67,9 +70,10 @@ def build_matrix(seed: int, layer: int, cfg: dict, name: str, scratch: Optional[
         sp = scales.data_ptr() + e * ssb
         moeq_synth_scales(seed, S.stream_id(layer, role, e, S.KIND_SCALES), fmt, rows * nb, sp)
         moe_pack_expert(fmt, rows, cols, scratch, sp, codes.data_ptr() + e * scb, sp)
-    books = np.stack([S.codebook(seed, S.stream_id(layer, role, e, S.KIND_CODEBOOK), fmt)
-                      for e in range(E)])
-    codebooks = torch.from_numpy(books.astype(np.int8)).to(device)
+    books = np.zeros((E, CB_STRIDE), dtype=np.int8)  # records padded to 16 bytes
+    for e in range(E):
+        books[e, : 1 << fmt] = S.codebook(seed, S.stream_id(layer, role, e, S.KIND_CODEBOOK), fmt)
+    codebooks = torch.from_numpy(books).to(device)
     return DeviceMatrix(fmt, rows, cols, E, codes, scales, codebooks, scb, ssb)
 
 

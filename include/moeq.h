@@ -72,9 +72,9 @@ typedef struct {
   size_t expert_stride_codes;   /* bytes, multiple of 16 */
   const void* scales;           /* 16-byte aligned */
   size_t expert_stride_scales;  /* bytes, multiple of 16 */
-  const int8_t* codebooks;      /* [num_experts] records of cb_len int8 */
+  const int8_t* codebooks;      /* [num_experts] records of cb_len int8; 16-byte aligned */
   int cb_len;                   /* must equal 2^fmt */
-  int cb_stride;                /* bytes between records, >= cb_len */
+  int cb_stride;                /* bytes between records: >= cb_len, multiple of 16 */
 } moeq_matrix;
 
 typedef struct {

@@ -47,7 +47,7 @@ def _mat(fmt, rows, cols, E, **kw):
     cb, sb = M.moeq_packed_bytes(fmt, rows, cols)
     d = dict(fmt=fmt, rows=rows, cols=cols, num_experts=E, codes=FAKE, expert_stride_codes=cb,
              scales=FAKE, expert_stride_scales=(sb + 15) // 16 * 16, codebooks=FAKE,
-             cb_len=1 << fmt, cb_stride=1 << fmt)
+             cb_len=1 << fmt, cb_stride=16)
     d.update(kw)
     return M.MoeqMatrix(**d)
 
@@ -70,7 +70,7 @@ def test_validation_codes():
     cases = {
         "MOEQ_ERR_CODEBOOK_MISSING": dict(gate=_mat(2, 256, 256, 16, codebooks=None)),
         "MOEQ_ERR_CODEBOOK_TRUNCATED": dict(down=_mat(3, 256, 256, 16, cb_len=4)),
-        "MOEQ_ERR_CODEBOOK_MISMATCH": dict(up=_mat(2, 256, 256, 16, cb_len=8, cb_stride=8)),
+        "MOEQ_ERR_CODEBOOK_MISMATCH": dict(up=_mat(2, 256, 256, 16, cb_len=8)),
         "MOEQ_ERR_CODEBOOK_DUPLICATE": dict(gate=_mat(2, 256, 256, 16, cb_stride=0)),
         "MOEQ_ERR_FORMAT": dict(gate=M.MoeqMatrix(5, 256, 256, 16, FAKE, 1 << 20, FAKE, 1 << 20,
                                                   FAKE, 32, 32)),
@@ -81,6 +81,11 @@ def test_validation_codes():
     for code, over in cases.items():
         assert M.moeq_validate_layer(_layer(**over)) == M.CODE[code], code
     assert M.moeq_validate_layer(_layer(k=17)) == M.CODE["MOEQ_ERR_ARG"]
+    # codebook records must be 16-byte aligned and strided
+    assert M.moeq_validate_layer(_layer(gate=_mat(2, 256, 256, 16, cb_stride=20))) == \
+        M.CODE["MOEQ_ERR_ALIGN"]
+    assert M.moeq_validate_layer(_layer(gate=_mat(2, 256, 256, 16, codebooks=FAKE + 4))) == \
+        M.CODE["MOEQ_ERR_ALIGN"]
     assert M.moe_ffn_workspace(_layer(H=200), 1, 0) == 0
     # a gate/up format mismatch is a format error
     assert M.moeq_validate_layer(_layer(up=_mat(4, 256, 256, 16))) == M.CODE["MOEQ_ERR_FORMAT"]

@@ -126,6 +126,6 @@ def test_decode_repeatable_and_workspace_reused():
         np.testing.assert_array_equal(ys[2 * rep + 1], ys[1])
     # counters are back to zero after every call
     ns = cfg["k"] + 1
-    n_ctr = 32 * (5 + ns) + 32 * 32   # counter lines, then the routing record copies
+    n_ctr = 32 * (4 + ns) + 32 * 16   # counter lines, then the routing record copies
     ctr = ws.buf[: 4 * n_ctr].view(torch.int32).cpu().numpy()
     assert not ctr.any()
