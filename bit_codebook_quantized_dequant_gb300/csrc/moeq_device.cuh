@@ -267,6 +267,42 @@ __device__ __forceinline__ int block_dot(const uint8_t* p, const uint32_t* cb, c
   }
 }
 
+// Expansion of one block into 8 words of int8 weights (v[i] = weights
+// 4i..4i+3), for blocks dotted with several activation vectors.
+template <int FMT>
+__device__ __forceinline__ void block_expand(const uint8_t* p, const uint32_t* cb, uint32_t (&v)[8]) {
+  if constexpr (FMT == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    const uint32_t a0 = w.x & 0x33333333u, b0 = (w.x >> 2) & 0x33333333u;
+    const uint32_t a1 = w.y & 0x33333333u, b1 = (w.y >> 2) & 0x33333333u;
+    v[0] = prmt(cb[0], cb[0], a0); v[1] = prmt(cb[0], cb[0], a0 >> 16);
+    v[2] = prmt(cb[0], cb[0], b0); v[3] = prmt(cb[0], cb[0], b0 >> 16);
+    v[4] = prmt(cb[0], cb[0], a1); v[5] = prmt(cb[0], cb[0], a1 >> 16);
+    v[6] = prmt(cb[0], cb[0], b1); v[7] = prmt(cb[0], cb[0], b1 >> 16);
+  } else if constexpr (FMT == 3) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+    const Fp3Sel t = fp3_selectors(w[0], w[1], w[2]);
+    v[0] = prmt(cb[0], cb[1], t.s00); v[1] = prmt(cb[0], cb[1], t.s00 >> 16);
+    v[2] = prmt(cb[0], cb[1], t.s01); v[3] = prmt(cb[0], cb[1], t.s01 >> 16);
+    v[4] = prmt(cb[0], cb[1], t.s10); v[5] = prmt(cb[0], cb[1], t.s10 >> 16);
+    v[6] = prmt(cb[0], cb[1], t.s11); v[7] = prmt(cb[0], cb[1], t.s11 >> 16);
+  } else {
+    const uint4 wd = *reinterpret_cast<const uint4*>(p);
+    fp4_expand(wd.x, cb[0], cb[1], cb[2], cb[3], v[0], v[1]);
+    fp4_expand(wd.y, cb[0], cb[1], cb[2], cb[3], v[2], v[3]);
+    fp4_expand(wd.z, cb[0], cb[1], cb[2], cb[3], v[4], v[5]);
+    fp4_expand(wd.w, cb[0], cb[1], cb[2], cb[3], v[6], v[7]);
+  }
+}
+
+// Dot product of an expanded block with 32 int8 activations (exact int32).
+__device__ __forceinline__ int dot8(const uint32_t (&v)[8], const int* q) {
+  int s = __dp4a(static_cast<int>(v[0]), q[0], 0);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) s = __dp4a(static_cast<int>(v[i]), q[i], s);
+  return s;
+}
+
 template <int FMT>
 __host__ __device__ constexpr int block_bytes() {
   return FMT == 2 ? 8 : FMT == 3 ? 12 : 16;

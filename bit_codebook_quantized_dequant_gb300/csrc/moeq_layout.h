@@ -4,6 +4,12 @@
 
 #include <stddef.h>
 
+#ifdef __CUDACC__
+#define MOEQ_HD __host__ __device__
+#else
+#define MOEQ_HD
+#endif
+
 namespace moeq {
 
 constexpr int kMaxTopK = 8;
@@ -14,12 +20,15 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // many CTAs poll or update has its own 128-byte line:
 //   kCtrQueue      work queue (items taken)
 //   kCtrRouter     router items done
-//   kCtrDownDone   down units done
+//   kCtrDownDone   down items done
 //   kCtrDone       CTAs finished (the last one resets the counters)
-//   kCtrHqDone + kCtrLine * s   quantized 32-blocks of h of slot s
-// followed by kRouteCopies copies of the routing record, one line each, every
-// copy read by a few CTAs only: idx[8], p[8] (fp32 bits), and a ready flag in
-// the last word, stored with release semantics after the rest of the line.
+//   kCtrHqDone + kCtrLine * u   quantized 32-blocks of h of unit u
+// followed by kRouteCopies copies of the routing record, every copy read by a
+// few CTAs only. A record is route_lines(cols) lines with a ready flag in the
+// last word, stored with release semantics after the rest of the record:
+//   1 column:  idx[8], p[8] (fp32 bits) in one line;
+//   4 columns: idx[c*8 + j], then p[c*8 + j], then the unit words, then the
+//              unit count in word 0 of the last line.
 constexpr int kCtrLine = 32;  // words per 128-byte line
 constexpr int kCtrQueue = 0;
 constexpr int kCtrRouter = 1 * kCtrLine;
@@ -28,35 +37,41 @@ constexpr int kCtrDone = 3 * kCtrLine;
 constexpr int kCtrHqDone = 4 * kCtrLine;
 constexpr int kRouteCopies = 16;
 constexpr int kRouteFlag = kCtrLine - 1;
-inline constexpr int route_base(int max_slots) { return kCtrHqDone + kCtrLine * max_slots; }
-inline constexpr int ctr_words(int max_slots) { return route_base(max_slots) + kCtrLine * kRouteCopies; }
+MOEQ_HD inline constexpr int route_lines(int cols) { return cols == 1 ? 1 : 4; }
+MOEQ_HD inline constexpr int route_base(int max_units) { return kCtrHqDone + kCtrLine * max_units; }
+MOEQ_HD inline constexpr int ctr_words(int max_units, int cols) {
+  return route_base(max_units) + kCtrLine * kRouteCopies * route_lines(cols);
+}
 
-// Bytes between the fp16 scales of h of consecutive slots (16-byte multiple so
-// that one slot's scales can be moved with a bulk copy).
+// Bytes between the fp16 scales of consecutive h vectors (16-byte multiple so
+// that they can be moved with bulk copies).
 inline size_t hd_stride(int I) { return (2 * static_cast<size_t>(I / 32) + 15) & ~static_cast<size_t>(15); }
 
+// Decode (cols = 1) and q=4 verification (cols = 4). A "unit" is one expert
+// whose weights are read once: up to cols*k distinct routed experts, then the
+// shared expert at index cols*k. h and the expert outputs are kept per (unit,
+// column): vector u*cols + c.
 struct DecodeWs {
-  int nslots;
+  int nunits, nvec;
   size_t ctr, n_ctr, logits, hq, hd, obuf, total;
 };
 
 inline DecodeWs decode_ws_layout(int H, int I, int E, int k, int has_shared, int cols = 1) {
   DecodeWs w;
-  // cols > 1 (q=4 verification): one slot per (column, routed choice) plus the shared expert
-  // per column; slot bookkeeping is the same.
-  w.nslots = cols * (k + (has_shared ? 1 : 0));
+  w.nunits = cols * k + (has_shared ? 1 : 0);
+  w.nvec = w.nunits * cols;
   size_t off = 0;
   w.ctr = off;
-  w.n_ctr = static_cast<size_t>(ctr_words(w.nslots));
+  w.n_ctr = static_cast<size_t>(ctr_words(w.nunits, cols));
   off += align256(4 * w.n_ctr);
   w.logits = off;
   off += align256(4 * static_cast<size_t>(cols) * E);
   w.hq = off;
-  off += align256(static_cast<size_t>(w.nslots) * I);
+  off += align256(static_cast<size_t>(w.nvec) * I);
   w.hd = off;
-  off += align256(hd_stride(I) * static_cast<size_t>(w.nslots));
+  off += align256(hd_stride(I) * static_cast<size_t>(w.nvec));
   w.obuf = off;
-  off += align256(4 * static_cast<size_t>(w.nslots) * H);
+  off += align256(4 * static_cast<size_t>(w.nvec) * H);
   w.total = off;
   return w;
 }

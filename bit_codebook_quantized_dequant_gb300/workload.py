@@ -145,7 +145,8 @@ class Workspace:
 
 
 class Debug:
-    """Device buffers for the intermediates of a decode (T tokens)."""
+    """Device buffers for the intermediates of a decode (T = 1) or of a q=4
+    verification (T = 4 columns); vectors are (column, slot) pairs."""
 
     def __init__(self, cfg: dict, T: int = 1, partials: bool = False, device="cuda"):
         H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["k"]
@@ -157,9 +158,9 @@ class Debug:
                       hq=z(T * ns * I, torch.int8), hd=z(T * ns * I // 32, torch.int16),
                       o=z(T * ns * H, torch.float32))
         if partials:
-            self.t.update(S_gate=z(ns * I * H // 32, torch.int32),
-                          S_up=z(ns * I * H // 32, torch.int32),
-                          S_down=z(ns * H * I // 32, torch.int32))
+            self.t.update(S_gate=z(T * ns * I * H // 32, torch.int32),
+                          S_up=z(T * ns * I * H // 32, torch.int32),
+                          S_down=z(T * ns * H * I // 32, torch.int32))
         self.struct = MoeqDebug(**{n: v.data_ptr() for n, v in self.t.items()})
 
     def numpy(self) -> Dict[str, np.ndarray]:

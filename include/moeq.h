@@ -89,7 +89,9 @@ typedef struct {
 } moeq_layer;
 
 /* Optional intermediates for parity tests; any pointer may be NULL. For
- * T tokens, "slots" = k routed experts followed by the shared one (if any). */
+ * T tokens (T = 1 for a decode, 4 columns for a q=4 verification), "slots" =
+ * k routed experts followed by the shared one (if any); vectors are ordered
+ * (token, slot). */
 typedef struct {
   int8_t* xq; uint16_t* xd;     /* [T x H], [T x H/32] quantized (rotated) input */
   float* logits;                /* [T x E] */
@@ -97,16 +99,16 @@ typedef struct {
   float* h;                     /* [T x slots x I] SwiGLU output before rotation */
   int8_t* hq; uint16_t* hd;     /* [T x slots x I], [T x slots x I/32] */
   float* o;                     /* [T x slots x H] expert outputs before the combine */
-  int32_t* S_gate, *S_up;       /* decode only: [slots x I x H/32] int32 block partials */
-  int32_t* S_down;              /* decode only: [slots x H x I/32] */
-  uint64_t* trace;              /* decode only: timeline, [grid x 4 roles x trace_cap x 2]
+  int32_t* S_gate, *S_up;       /* decode / q=4: [T x slots x I x H/32] int32 block partials */
+  int32_t* S_down;              /* decode / q=4: [T x slots x H x I/32] */
+  uint64_t* trace;              /* decode / q=4: timeline, [grid x 4 roles x trace_cap x 2]
                                    of (globaltimer ns, event << 32 | unit); see MOEQ_TRACE_* */
   int trace_cap;                /* events per (CTA, role) */
 } moeq_debug;
 
-/* Timeline events of moe_ffn_decode (role 0 = compute group 0, 1 = producer
- * warp, 2 = epilogue warp, 3 = compute group 1). Unused entries stay as the
- * caller left them. */
+/* Timeline events of moe_ffn_decode and moe_ffn_verify_q4 (role 0 = compute
+ * group 0, 1 = producer warp, 3 = compute group 1; role 2 is not used).
+ * Unused entries stay as the caller left them. */
 enum {
   MOEQ_TRACE_START = 1,      /* compute: x quantized; producer: first unit taken */
   MOEQ_TRACE_TAKE = 2,       /* producer: unit taken from the queue */
@@ -171,17 +173,24 @@ int moe_route_topk(const uint16_t* x, int T, const uint16_t* router, int E, int 
  * moe_ffn_workspace(L, 1, 0) bytes, zeroed once with moe_ffn_workspace_init;
  * calls that share a workspace must be ordered (same stream). dbg may be NULL.
  * Requires H <= 4096 and a multiple of 256, I <= 4096 and a multiple of 128,
- * E <= 512 and a multiple of 8; k <= 8. */
+ * E <= 512 and a multiple of 4; k <= 8. */
 int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, void* ws, size_t ws_bytes,
                    int32_t* dev_status, const moeq_debug* dbg, moeq_stream stream);
 
 /* q=4 verification ("DeepSeek V4 Flash: 284B model ...", section "Decode: up
- * to 32 tok/s"): four columns x [4 x H], each routed independently,
- * y [4 x H] = the decode of each column; every packed block of every expert,
- * of the shared expert and of the optional dense FP4 [H x H] projection is
- * expanded once per call and applied to every column that uses it;
- * y_dense [4 x H] = dense * Q8(column) (NULL dense -> y_dense untouched).
- * ws: moe_ffn_workspace(L, 4, 1) bytes. */
+ * to 32 tok/s": the verifier decodes each packed weight once and applies it
+ * to all four columns): four columns x [4 x H] bf16, each routed
+ * independently; y [4 x H] fp32 = the decode of each column, bit for bit
+ * what four moe_ffn_decode calls return. Every packed block of every selected
+ * expert (read once for all columns that select it), of the shared expert and
+ * of the optional dense projection is expanded once per call and applied to
+ * every column that uses it. dense: NULL or one matrix [D x H] (any format,
+ * D % 32 == 0, one codebook record); y_dense [4 x D] fp32 = dense applied to
+ * the column's quantized (and, with h32_signs_x, rotated) input -- the same
+ * Q8 operand as the FFN; with dense NULL y_dense is not touched and may be
+ * NULL. One persistent cooperative kernel. ws: moe_ffn_workspace(L, 4, 1)
+ * bytes, zeroed once; calls that share a workspace must be ordered. Same shape
+ * limits as moe_ffn_decode. */
 int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, const uint16_t* x, float* y,
                       float* y_dense, void* ws, size_t ws_bytes, int32_t* dev_status,
                       const moeq_debug* dbg, moeq_stream stream);

@@ -60,3 +60,56 @@ def check_output(y_gpu, y_ref, bound, what=""):
     assert np.all(err <= ELEM * bound), f"{what}: max |err|/B = {worst:.3g} > {ELEM}"
     assert rel <= REL_L2, f"{what}: relative L2 {rel:.3g} > {REL_L2}"
     return worst, rel
+
+
+def check_token(L, cfg, x_row, y, g, partials):
+    """Stage-by-stage parity of one token's decode intermediates g (one
+    column's view of the debug buffers) and output y against the oracle.
+    Returns the independent oracle output, the bound B and whether the GPU's
+    quantized h equals the oracle's."""
+    H, I, k = cfg["H"], cfg["I"], cfg["k"]
+    ns = k + (1 if cfg["shared_fmt"] else 0)
+    yo, tr = O.ffn_decode(L, x_row, trace=True, partials=partials)
+    np.testing.assert_array_equal(g["xq"], tr["xq"])
+    np.testing.assert_array_equal(g["xd"], tr["xd"])
+    np.testing.assert_array_equal(g["logits"], tr["logits"])
+    np.testing.assert_array_equal(g["idx"], tr["idx"])
+    np.testing.assert_allclose(g["p"], tr["p"], rtol=2e-6)
+    h = g["h"].reshape(ns, I)
+    np.testing.assert_allclose(h, tr["h"][:ns], rtol=2e-4, atol=2e-6 * np.abs(tr["h"][:ns]).max())
+    # quantization decision: the oracle's quantizer on the GPU's h, bit for bit
+    hq = g["hq"].reshape(ns, I)
+    hd = g["hd"].reshape(ns, I // 32)
+    for s in range(ns):
+        hh = h[s]
+        if L.signs_h is not None:
+            hh = O.h32_f32(hh, L.signs_h)
+        q, d = O.q8(hh)
+        np.testing.assert_array_equal(hq[s], q)
+        np.testing.assert_array_equal(hd[s], d)
+    # independent quantization differs at most by one step, on rare elements
+    diff = np.abs(hq.astype(int) - tr["hq"][:ns].astype(int))
+    assert diff.max() <= 1 and (diff > 0).sum() <= max(2, 1e-3 * diff.size)
+    # teacher-forced down projection: bit-exact partials, tight y
+    yt, tt = O.ffn_decode(L, x_row, trace=True, partials=partials, force_hq=hq, force_hd=hd)
+    if partials:
+        np.testing.assert_array_equal(g["S_gate"].reshape(ns, I, H // 32), tr["S_gate"][:ns])
+        np.testing.assert_array_equal(g["S_up"].reshape(ns, I, H // 32), tr["S_up"][:ns])
+        np.testing.assert_array_equal(g["S_down"].reshape(ns, H, I // 32), tt["S_down"][:ns])
+    B = output_bound(L, tr["idx"], tr["p"], hq, hd)
+    o = g["o"].reshape(ns, H)
+    for s, bs in enumerate(slot_bounds(L, tr["idx"], hq, hd)):
+        assert np.all(np.abs(o[s] - tt["o"][s]) <= 1e-5 * bs), f"o[{s}]"
+    check_output(y, yt, B, "y (teacher-forced)")
+    same_q = np.array_equal(hq, tr["hq"][:ns]) and np.array_equal(hd, tr["hd"][:ns])
+    return yo, B, same_q
+
+
+def column_view(g, cfg, c):
+    """The debug buffers of column c of a multi-column call, shaped like a
+    single-token decode's."""
+    H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["k"]
+    ns = k + (1 if cfg["shared_fmt"] else 0)
+    per = dict(xq=H, xd=H // 32, logits=E, idx=k, p=k, h=ns * I, hq=ns * I, hd=ns * I // 32,
+               o=ns * H, S_gate=ns * I * H // 32, S_up=ns * I * H // 32, S_down=ns * H * I // 32)
+    return {n: v[c * per[n]:(c + 1) * per[n]] for n, v in g.items()}

@@ -107,5 +107,17 @@ def test_entry_points_reject_bad_arguments_before_launch():
         M.CODE["MOEQ_ERR_SHAPE"]
     assert lib.moe_route_topk(FAKE, 1, FAKE, 16, 256, 9, FAKE, FAKE, None, None, None) == \
         M.CODE["MOEQ_ERR_ARG"]
+    # q=4 verification: dense projection shape, its output and the workspace
+    dense_bad = _mat(4, 256, 512, 1)   # cols != H
+    dense_ok = _mat(4, 256, 256, 1)
+    assert lib.moe_ffn_verify_q4(C.byref(L), C.byref(dense_bad), FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                                 None, None, None) == M.CODE["MOEQ_ERR_SHAPE"]
+    assert lib.moe_ffn_verify_q4(C.byref(L), C.byref(dense_ok), FAKE, FAKE, None, FAKE, 1 << 30,
+                                 None, None, None) == M.CODE["MOEQ_ERR_ARG"]
+    assert lib.moe_ffn_verify_q4(C.byref(L), None, FAKE, FAKE, None, FAKE, 16, None, None,
+                                 None) == M.CODE["MOEQ_ERR_WORKSPACE"]
+    need4 = lib.moe_ffn_workspace(C.byref(L), 4, 1)
+    need1 = lib.moe_ffn_workspace(C.byref(L), 1, 0)
+    assert need4 > need1 > 0
     assert lib.h32_rotate(None, None, 4, None, None) == M.CODE["MOEQ_ERR_ARG"]
     assert lib.moe_rmsnorm_bf16(FAKE, 1, 100, FAKE, None) == M.CODE["MOEQ_ERR_SHAPE"]

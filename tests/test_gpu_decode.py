@@ -11,7 +11,7 @@ import bit_codebook_quantized_dequant_gb300 as M
 from bit_codebook_quantized_dequant_gb300 import synth as S
 from bit_codebook_quantized_dequant_gb300.workload import (Debug, Workspace, build_layer,
                                                            to_dev_u16)
-from _parity import check_output, host_layer_for, output_bound, slot_bounds
+from _parity import check_output, check_token, host_layer_for
 
 pytestmark = pytest.mark.gpu
 
@@ -33,45 +33,6 @@ def _run(dl, ws, x_row, partials):
     return y.cpu().numpy(), dbg.numpy()
 
 
-def _check_token(L, cfg, x_row, y, g, partials):
-    H, I, k = cfg["H"], cfg["I"], cfg["k"]
-    ns = k + (1 if cfg["shared_fmt"] else 0)
-    yo, tr = O.ffn_decode(L, x_row, trace=True, partials=partials)
-    np.testing.assert_array_equal(g["xq"], tr["xq"])
-    np.testing.assert_array_equal(g["xd"], tr["xd"])
-    np.testing.assert_array_equal(g["logits"], tr["logits"])
-    np.testing.assert_array_equal(g["idx"], tr["idx"])
-    np.testing.assert_allclose(g["p"], tr["p"], rtol=2e-6)
-    h = g["h"].reshape(ns, I)
-    np.testing.assert_allclose(h, tr["h"][:ns], rtol=2e-4, atol=2e-6 * np.abs(tr["h"][:ns]).max())
-    # quantization decision: the oracle's quantizer on the GPU's h, bit for bit
-    hq = g["hq"].reshape(ns, I)
-    hd = g["hd"].reshape(ns, I // 32)
-    for s in range(ns):
-        hh = h[s]
-        if L.signs_h is not None:
-            hh = O.h32_f32(hh, L.signs_h)
-        q, d = O.q8(hh)
-        np.testing.assert_array_equal(hq[s], q)
-        np.testing.assert_array_equal(hd[s], d)
-    # independent quantization differs at most by one step, on rare elements
-    diff = np.abs(hq.astype(int) - tr["hq"][:ns].astype(int))
-    assert diff.max() <= 1 and (diff > 0).sum() <= max(2, 1e-3 * diff.size)
-    # teacher-forced down projection: bit-exact partials, tight y
-    yt, tt = O.ffn_decode(L, x_row, trace=True, partials=partials, force_hq=hq, force_hd=hd)
-    if partials:
-        np.testing.assert_array_equal(g["S_gate"].reshape(ns, I, H // 32), tr["S_gate"][:ns])
-        np.testing.assert_array_equal(g["S_up"].reshape(ns, I, H // 32), tr["S_up"][:ns])
-        np.testing.assert_array_equal(g["S_down"].reshape(ns, H, I // 32), tt["S_down"][:ns])
-    B = output_bound(L, tr["idx"], tr["p"], hq, hd)
-    o = g["o"].reshape(ns, H)
-    for s, bs in enumerate(slot_bounds(L, tr["idx"], hq, hd)):
-        assert np.all(np.abs(o[s] - tt["o"][s]) <= 1e-5 * bs), f"o[{s}]"
-    check_output(y, yt, B, "y (teacher-forced)")
-    same_q = np.array_equal(hq, tr["hq"][:ns]) and np.array_equal(hd, tr["hd"][:ns])
-    return yo, B, same_q
-
-
 @pytest.mark.parametrize("variant", ["cfg0", "cfg0-shared", "cfg0-h32-fp4", "cfg0-fp2-down"])
 def test_decode_tiny(variant):
     over = {}
@@ -89,7 +50,7 @@ def test_decode_tiny(variant):
     L = host_layer_for(seed, 0, cfg, xs)
     for t in range(xs.shape[0]):
         y, g = _run(dl, ws, xs[t], partials=True)
-        yo, B, same_q = _check_token(L, cfg, xs[t], y, g, partials=True)
+        yo, B, same_q = check_token(L, cfg, xs[t], y, g, partials=True)
         if same_q:  # no fp32-vs-fp64 rounding of h crossed a quantization step
             check_output(y, yo, B, "y (independent)")
 
@@ -103,7 +64,7 @@ def test_decode_config1_sampled_tokens():
     L = host_layer_for(seed, 0, cfg, xs)
     for t in range(xs.shape[0]):
         y, g = _run(dl, ws, xs[t], partials=(t == 0))
-        _check_token(L, cfg, xs[t], y, g, partials=(t == 0))
+        check_token(L, cfg, xs[t], y, g, partials=(t == 0))
 
 
 def test_decode_repeatable_and_workspace_reused():
