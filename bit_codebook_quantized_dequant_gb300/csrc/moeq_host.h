@@ -57,4 +57,8 @@ const DeviceInfo& device_info();
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOEQ_ERR_CUDA; }
 
+// Router + top-k of T tokens enqueued on s (route.cu).
+int route_topk_launch(const uint16_t* x, int T, const uint16_t* router, int E, int H, int k,
+                      int32_t* idx, float* w, float* logits, cudaStream_t s);
+
 }  // namespace moeq

@@ -80,28 +80,34 @@ inline DecodeWs verify_ws_layout(int H, int I, int E, int k, int has_shared) {
   return decode_ws_layout(H, I, E, k, has_shared, 4);
 }
 
-// Prefill workspace for up to T tokens.
+// Prefill workspace for up to T tokens. Groups: the E routed experts, then
+// the shared expert (if any). Grouped rows: the (token, slot) pairs of every
+// routed expert in a stable order (ascending token, then slot), then the T
+// rows of the shared expert. pid[row] = token * k + slot for routed rows and
+// T * k + token for shared rows; pos[token * k + slot] = its row.
 struct PrefillWs {
-  size_t xq, xd, idx, p, counts, offsets, perm, pos, hq, hd, o, total;
+  size_t xq, xd, idx, p, counts, offsets, tiles_gu, tiles_dn, pid, pos, hq, hd, o, total;
 };
 
 inline PrefillWs prefill_ws_layout(int H, int I, int E, int k, int has_shared, int T) {
   PrefillWs w;
   const size_t Tk = static_cast<size_t>(T) * k;
-  const size_t rows = Tk + (has_shared ? static_cast<size_t>(T) : 0);  // grouped rows incl. shared
-  const int groups = E + (has_shared ? 1 : 0);
+  const size_t rows = Tk + (has_shared ? static_cast<size_t>(T) : 0);
+  const size_t groups = static_cast<size_t>(E) + (has_shared ? 1 : 0);
   size_t off = 0;
-  w.xq = off;      off += align256(static_cast<size_t>(T) * H);
-  w.xd = off;      off += align256(2 * static_cast<size_t>(T) * (H / 32));
-  w.idx = off;     off += align256(4 * Tk);
-  w.p = off;       off += align256(4 * Tk);
-  w.counts = off;  off += align256(4 * static_cast<size_t>(groups + 1) * 2);
-  w.offsets = off; off += align256(4 * static_cast<size_t>(groups + 1));
-  w.perm = off;    off += align256(4 * rows);
-  w.pos = off;     off += align256(4 * Tk);
-  w.hq = off;      off += align256(rows * I);
-  w.hd = off;      off += align256(2 * rows * (I / 32));
-  w.o = off;       off += align256(4 * rows * H);
+  w.xq = off;       off += align256(static_cast<size_t>(T) * H);
+  w.xd = off;       off += align256(2 * static_cast<size_t>(T) * (H / 32));
+  w.idx = off;      off += align256(4 * Tk);
+  w.p = off;        off += align256(4 * Tk);
+  w.counts = off;   off += align256(4 * (groups + 1));
+  w.offsets = off;  off += align256(4 * (groups + 1));
+  w.tiles_gu = off; off += align256(4 * (groups + 1));
+  w.tiles_dn = off; off += align256(4 * (groups + 1));
+  w.pid = off;      off += align256(4 * rows);
+  w.pos = off;      off += align256(4 * Tk);
+  w.hq = off;       off += align256(rows * I);
+  w.hd = off;       off += align256(2 * rows * (I / 32));
+  w.o = off;        off += align256(4 * rows * H);
   w.total = off;
   return w;
 }

@@ -197,12 +197,16 @@ int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, const uint1
 
 /* Expert-grouped prefill of T tokens ("deepseek-v4-flash-0731-evox3-rocm",
  * section "The optimization ladder": fused multi-token prefill): per token
- * the same result as moe_ffn_decode, computed as router + top-k for all
- * tokens, a stable counting sort of (token, slot) pairs by expert, grouped
- * GEMMs for gate/up (+SwiGLU, H32, Q8 of h) and down, and a gather-combine in
- * slot order. If residual is not NULL, y = residual + FFN(x) (the residual
- * add of a stacked layer; y may equal residual). x [T x H] bf16, y [T x H]
- * fp32. ws: moe_ffn_workspace(L, T, 2) bytes. */
+ * the same result as moe_ffn_decode up to fp32 summation order, computed as
+ * router + top-k for all tokens, a stable counting sort of the (token, slot)
+ * pairs by expert (ascending token, then slot), grouped GEMMs for gate/up
+ * (+SwiGLU, H32, Q8 of h) and down, and a gather-combine in slot order. If
+ * residual is not NULL, y = residual + FFN(x) rounded once (the residual add
+ * of a stacked layer; y may equal residual). x [T x H] bf16, y [T x H] fp32.
+ * ws: at least moe_ffn_workspace(L, T, 2) bytes (contents need no zeroing);
+ * too small -> MOEQ_ERR_WORKSPACE. T = 0 enqueues nothing. Several kernels
+ * on the stream, no host synchronization; dbg (NULL or [T x slots] vectors)
+ * receives xq, xd, logits, idx, p, h, hq, hd and o. */
 int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, const float* residual, float* y,
                     void* ws, size_t ws_bytes, int32_t* dev_status, const moeq_debug* dbg,
                     moeq_stream stream);
