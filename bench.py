@@ -47,6 +47,24 @@ def algorithmic_bytes_decode(cfg: dict) -> int:
     return E * H * 2 + k * routed + shared
 
 
+def algorithmic_bytes_verify(cfg: dict, distinct_experts: float) -> float:
+    """Packed weight bytes one q=4 call reads: router, each distinct routed
+    expert once, the shared expert and the dense projection once."""
+    H, I, E = cfg["H"], cfg["I"], cfg["E"]
+    per_blk = {2: 10, 3: 14, 4: 17}
+    routed = 2 * I * (H // 32) * per_blk[cfg["fmt_gu"]] + H * (I // 32) * per_blk[cfg["fmt_down"]]
+    shared = 3 * I * (H // 32) * per_blk[cfg["shared_fmt"]] if cfg["shared_fmt"] else 0
+    dense = H * (H // 32) * per_blk[4] if cfg["dense"] else 0
+    return E * H * 2 + distinct_experts * routed + shared + dense
+
+
+def prefill_flops(cfg: dict, T: int) -> float:
+    """Expert FLOPs of a prefill of T tokens: 3 matrices of H x I per routed
+    slot and for the shared expert, 2 FLOPs per multiply-add."""
+    ns = cfg["k"] + (1 if cfg["shared_fmt"] else 0)
+    return 2.0 * T * ns * 3 * cfg["H"] * cfg["I"]
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -177,6 +195,121 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def _timed(fn, warmup, steps, stream):
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        fn(warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def bench_verify(args, hbm_peak, peak_kind):
+    """q=4 verification: 4 columns per call through moe_ffn_verify_q4, cycling
+    over 2 seeded layer replicas (each with its dense projection)."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, to_dev_u16
+    cid = 2
+    cfg = S.CONFIGS[cid]
+    seed = S.config_seed(cid)
+    R = 2
+    layers = [build_layer(seed, r, cfg) for r in range(R)]
+    wss = [Workspace(dl, 1) for dl in layers]
+    descs = [dl.desc() for dl in layers]
+    dds = [dl.dense.desc() for dl in layers]
+    nb = 64
+    X = S.tokens(seed, cfg, 4 * nb)
+    xs = to_dev_u16(X)
+    H = cfg["H"]
+    y = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
+    yd = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        r = i % R
+        M.moe_ffn_verify_q4(descs[r], dds[r], xs.data_ptr() + (i % nb) * 4 * H * 2, y, yd,
+                            wss[r].ptr, wss[r].nbytes, st, None, stream)
+
+    steps = max(args.steps // 4, 50)
+    ms = _timed(step, args.warmup, steps, stream)
+    assert st.item() == 0, f"device status {st.item()}"
+    # distinct experts per call (routing of the same columns, outside the timed region)
+    distinct = []
+    idx = torch.zeros(4 * cfg["k"], dtype=torch.int32, device="cuda")
+    w = torch.zeros(4 * cfg["k"], dtype=torch.float32, device="cuda")
+    for r in range(R):
+        for b in range(nb):
+            M.moe_route_topk(xs.data_ptr() + b * 4 * H * 2, 4, layers[r].router, cfg["E"], H,
+                             cfg["k"], idx, w)
+            distinct.append(len(set(idx.cpu().tolist())))
+    nd = float(np.mean(distinct))
+    per_call = algorithmic_bytes_verify(cfg, nd)
+    achieved = per_call / (ms * 1e-3) / 1e9
+    out = {"metric": "q=4 verification column-tokens/s", "value": 4.0 / (ms * 1e-3),
+           "unit": "column-tok/s", "ms_per_call": ms, "calls": steps,
+           "workload": "verify-q4: decode-b1 layer + dense 4096x4096 FP4; 4 independently routed "
+                       "columns per call; 2 replicas cycled",
+           "distinct_experts_per_call": nd,
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": achieved / hbm_peak,
+                        "traffic": _traffic("ffn_kernel<4>",
+                                            "bit_codebook_quantized_dequant_gb300/csrc/decode.cu"),
+                        "peak_source": f"{peak_kind} hbm_gbs",
+                        "algorithmic_bytes_per_launch": per_call},
+           "gpu_launches": steps}
+    del layers, wss
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_prefill(args, cid, T, tc_peak, hbm_peak, peak_kind):
+    """Expert-grouped prefill of T tokens through one layer (moe_ffn_prefill)."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, to_dev_u16
+    cfg = S.CONFIGS[cid]
+    seed = S.config_seed(cid)
+    dl = build_layer(seed, 0, cfg)
+    ws = Workspace(dl, 2, T)
+    X = to_dev_u16(S.tokens(seed, cfg, T))
+    y = torch.zeros(T * cfg["H"], dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    desc = dl.desc()
+
+    def step(i):
+        M.moe_ffn_prefill(desc, X, T, None, y, ws.ptr, ws.nbytes, st, None, stream)
+
+    steps = 3
+    ms = _timed(step, 3, steps, stream)
+    assert st.item() == 0, f"device status {st.item()}"
+    fl = prefill_flops(cfg, T)
+    tflops = fl / (ms * 1e-3) / 1e12
+    wbytes = dl.weight_bytes()
+    out = {"metric": "prefill tok/s (one layer)", "value": T / (ms * 1e-3), "unit": "tok/s",
+           "ms_per_call": ms, "calls": steps, "tokens": T,
+           "workload": S.CONFIGS[cid]["name"] + f": T={T}, all 256 experts' weights read once",
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                        "frac": tflops / tc_peak, "traffic": None,
+                        "peak_source": f"{peak_kind} bf16_tflops (the prefill contraction runs "
+                                       "bf16-exact integer products)",
+                        "algorithmic_flops_per_launch": fl,
+                        "hbm_frac_weights": wbytes / (ms * 1e-3) / 1e9 / hbm_peak},
+           "gpu_launches_per_call": 10}
+    del dl, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run(args):
     import torch
     import bit_codebook_quantized_dequant_gb300 as M
@@ -260,7 +393,7 @@ def run(args):
             dist.destroy_process_group()
         return
 
-    hbm_peak, _, peak_kind = _peaks()
+    hbm_peak, tc_peak, peak_kind = _peaks()
     per_tok = algorithmic_bytes_decode(cfg)
     ms_step = ms / args.steps
     achieved = per_tok / (ms_step * 1e-3) / 1e9
@@ -270,7 +403,15 @@ def run(args):
     if world == 1 and not args.no_cpu_baseline:
         tps, sample, _ = cpu_baseline(CFG_ID, 20)
         cpu = {"value": tps, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample}
-    traffic = _traffic("decode_kernel", "bit_codebook_quantized_dequant_gb300/csrc/decode.cu")
+    traffic = _traffic("ffn_kernel<1>", "bit_codebook_quantized_dequant_gb300/csrc/decode.cu")
+    wbytes = R * layers[0].weight_bytes()
+    extra = {}
+    if world == 1 and not args.decode_only:
+        del layers, wss
+        torch.cuda.empty_cache()
+        extra["verify_q4"] = bench_verify(args, hbm_peak, peak_kind)
+        extra["prefill"] = [bench_prefill(args, 3, 2048, tc_peak, hbm_peak, peak_kind),
+                            bench_prefill(args, 4, 32512, tc_peak, hbm_peak, peak_kind)]
     line = {
         "metric": "MoE-FFN decode tok/s (batch 1, one layer)",
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -279,7 +420,7 @@ def run(args):
         "data": "synthetic (seeded SplitMix64 codes, scales, codebooks; x ~ N(0,1) bf16)",
         "config": {"workload": WORKLOAD, "replicas": R,
                    "l2": f"inputs larger than L2: {R} independently seeded layer replicas "
-                         f"({R * layers[0].weight_bytes() / 1e9:.1f} GB), cycled per step",
+                         f"({wbytes / 1e9:.1f} GB), cycled per step",
                    "tokens": ntok},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
@@ -291,6 +432,7 @@ def run(args):
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
+    line.update(extra)
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
@@ -304,6 +446,8 @@ def main():
     ap.add_argument("--replicas", type=int, default=8)
     ap.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time the decode workload only (no q=4 or prefill sections)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -92,6 +92,7 @@ def _declare(L):
                                   C.POINTER(MoeqDebug), P]),
         "moe_ffn_prefill": (i, [C.POINTER(MoeqLayer), P, i, P, P, P, sz, P, C.POINTER(MoeqDebug),
                                 P]),
+        "moe_ffn_stack_prefill": (i, [P, i, P, i, P, P, sz, P, P]),
         "h32_rotate": (i, [P, P, i, P, P]),
         "moe_rmsnorm_bf16": (i, [P, i, i, P, P]),
         "moeq_version": (C.c_char_p, []),
@@ -106,7 +107,8 @@ def _declare(L):
 
 EXPORTED = ["moeq_packed_bytes", "moeq_validate_layer", "moe_ffn_workspace",
             "moe_ffn_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_ffn_decode",
-            "moe_ffn_verify_q4", "moe_ffn_prefill", "h32_rotate", "moe_rmsnorm_bf16",
+            "moe_ffn_verify_q4", "moe_ffn_prefill", "moe_ffn_stack_prefill", "h32_rotate",
+            "moe_rmsnorm_bf16",
             "moeq_version", "moeq_synth_codes", "moeq_synth_scales"]
 
 
@@ -184,6 +186,14 @@ def moe_ffn_prefill(layer: MoeqLayer, x, T, residual, y, ws, ws_bytes, dev_statu
     return _check("moe_ffn_prefill", load().moe_ffn_prefill(
         C.byref(layer), _ptr(x), T, _ptr(residual), _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status),
         C.byref(dbg) if dbg is not None else None, _stream(stream)))
+
+
+def moe_ffn_stack_prefill(layers, x, T, r, ws, ws_bytes, dev_status=None, stream=None):
+    """layers: a sequence of MoeqLayer (copied into one contiguous array)."""
+    arr = (MoeqLayer * len(layers))(*layers)
+    return _check("moe_ffn_stack_prefill", load().moe_ffn_stack_prefill(
+        arr, len(layers), _ptr(x), T, _ptr(r), _ptr(ws), ws_bytes, _ptr(dev_status),
+        _stream(stream)))
 
 
 def h32_rotate(inp, out, nblk, signs=None, stream=None):

@@ -92,6 +92,9 @@ extern "C" size_t moe_ffn_workspace(const moeq_layer* L, int T_max, int mode) {
   if (mode == 0) return decode_ws_layout(L->H, L->I, L->E, L->k, L->has_shared).total;
   if (mode == 1) return verify_ws_layout(L->H, L->I, L->E, L->k, L->has_shared).total;
   if (mode == 2) return prefill_ws_layout(L->H, L->I, L->E, L->k, L->has_shared, T_max).total;
+  if (mode == 3)  // a stack of layers shaped like L: prefill workspace + the bf16 RMSNorm output
+    return prefill_ws_layout(L->H, L->I, L->E, L->k, L->has_shared, T_max).total +
+           align256(2 * static_cast<size_t>(T_max) * L->H);
   return 0;
 }
 

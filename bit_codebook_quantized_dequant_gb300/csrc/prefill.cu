@@ -463,6 +463,12 @@ __global__ void combine_kernel(const PrefillArgs a) {
   reinterpret_cast<float4*>(a.y + static_cast<size_t>(t) * a.H)[c] = acc;
 }
 
+// r = float(x) for a bf16 [n] input.
+__global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ x, float* __restrict__ r, size_t n) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) r[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+}
+
 template <int FMT>
 int launch_gu(const PrefillArgs& a, int g0, int g1, int shared, int grid, cudaStream_t s) {
   const int smem = static_cast<int>(sizeof(GemmSmem<FMT>));
@@ -567,4 +573,36 @@ extern "C" int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, co
   const size_t nout = static_cast<size_t>(T) * (L->H / 4);
   combine_kernel<<<static_cast<unsigned>((nout + 255) / 256), 256, 0, s>>>(a);
   return cuda_status(cudaGetLastError());
+}
+
+extern "C" int moe_ffn_stack_prefill(const moeq_layer* layers, int nlayers, const uint16_t* x, int T,
+                                     float* r, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                     moeq_stream stream) {
+  if (!layers || nlayers < 1) return MOEQ_ERR_ARG;
+  if (T < 0) return MOEQ_ERR_SHAPE;
+  const int H = layers[0].H;
+  size_t need = 0;
+  for (int l = 0; l < nlayers; ++l) {
+    const int rc = validate_layer(&layers[l]);
+    if (rc) return rc;
+    if (layers[l].H != H) return MOEQ_ERR_SHAPE;
+    const PrefillWs wl = prefill_ws_layout(layers[l].H, layers[l].I, layers[l].E, layers[l].k,
+                                           layers[l].has_shared, T);
+    need = wl.total > need ? wl.total : need;
+  }
+  if (T == 0) return MOEQ_OK;
+  if (!x || !r) return MOEQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(r)) return MOEQ_ERR_ALIGN;
+  const size_t abytes = align256(2 * static_cast<size_t>(T) * H);
+  if (!ws || !aligned16(ws) || ws_bytes < need + abytes) return MOEQ_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint16_t* a = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + need);
+  const size_t n = static_cast<size_t>(T) * H;
+  bf16_to_f32_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(x, r, n);
+  int rc = cuda_status(cudaGetLastError());
+  for (int l = 0; l < nlayers && !rc; ++l) {
+    rc = moe_rmsnorm_bf16(r, T, H, a, stream);
+    if (!rc) rc = moe_ffn_prefill(&layers[l], a, T, r, r, ws, need, dev_status, nullptr, stream);
+  }
+  return rc;
 }

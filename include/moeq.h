@@ -134,7 +134,8 @@ int moeq_packed_bytes(int fmt, int rows, int cols, size_t* code_bytes, size_t* s
 int moeq_validate_layer(const moeq_layer* L);
 
 /* Workspace bytes for a call: mode 0 = decode, 1 = q=4 verify, 2 = prefill of
- * up to T_max tokens. 0 on an invalid descriptor. */
+ * up to T_max tokens, 3 = moe_ffn_stack_prefill of up to T_max tokens through
+ * layers shaped like L. 0 on an invalid descriptor. */
 size_t moe_ffn_workspace(const moeq_layer* L, int T_max, int mode);
 
 /* Zero a freshly allocated workspace (enqueued memset). Needed once; every
@@ -210,6 +211,18 @@ int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, const uint1
 int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, const float* residual, float* y,
                     void* ws, size_t ws_bytes, int32_t* dev_status, const moeq_debug* dbg,
                     moeq_stream stream);
+
+/* Prefill of T tokens through a stack of nlayers layers (layers[l], all with
+ * the same H) with an fp32 residual stream ("Lucebox x Geometric ...",
+ * section "How the model fits": the prompt is pushed layer by layer through
+ * the whole stack):
+ *   r_0 = float(x);  a_l = moe_rmsnorm_bf16(r_l);  r_{l+1} = r_l + FFN_l(a_l)
+ * with FFN_l = moe_ffn_prefill of layer l (residual form, in place). x [T x H]
+ * bf16; r [T x H] fp32 receives r_nlayers. ws: at least
+ * moe_ffn_workspace(L, T, 3) bytes for the largest layer shape. Enqueued on
+ * the stream, no host synchronization. */
+int moe_ffn_stack_prefill(const moeq_layer* layers, int nlayers, const uint16_t* x, int T, float* r,
+                          void* ws, size_t ws_bytes, int32_t* dev_status, moeq_stream stream);
 
 /* H32 rotation ("deepseek-v4-flash-0731-evox3-rocm", section "The optimization
  * ladder"): out = H D in per 32-block, H the 32x32 Sylvester Hadamard matrix
