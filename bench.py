@@ -310,6 +310,22 @@ def bench_prefill(args, cid, T, tc_peak, hbm_peak, peak_kind):
     return out
 
 
+def run_sections(args, hbm_peak, tc_peak, peak_kind):
+    """The q=4 verification and prefill sections named in --sections."""
+    sec = args.sections.split(",")
+    out = {}
+    if "verify" in sec:
+        out["verify_q4"] = bench_verify(args, hbm_peak, peak_kind)
+    pre = []
+    if "prefill" in sec or "prefill3" in sec:
+        pre.append(bench_prefill(args, 3, 2048, tc_peak, hbm_peak, peak_kind))
+    if "prefill" in sec or "prefill4" in sec:
+        pre.append(bench_prefill(args, 4, 32512, tc_peak, hbm_peak, peak_kind))
+    if pre:
+        out["prefill"] = pre
+    return out
+
+
 def run(args):
     import torch
     import bit_codebook_quantized_dequant_gb300 as M
@@ -318,6 +334,12 @@ def run(args):
 
     world, rank, local = _dist()
     torch.cuda.set_device(local)
+    if "decode" not in args.sections.split(","):
+        # profiling runs of single sections (no headline line)
+        M.load()
+        hbm_peak, tc_peak, peak_kind = _peaks()
+        print(json.dumps(run_sections(args, hbm_peak, tc_peak, peak_kind)))
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -406,12 +428,10 @@ def run(args):
     traffic = _traffic("ffn_kernel<1>", "bit_codebook_quantized_dequant_gb300/csrc/decode.cu")
     wbytes = R * layers[0].weight_bytes()
     extra = {}
-    if world == 1 and not args.decode_only:
+    if world == 1:
         del layers, wss
         torch.cuda.empty_cache()
-        extra["verify_q4"] = bench_verify(args, hbm_peak, peak_kind)
-        extra["prefill"] = [bench_prefill(args, 3, 2048, tc_peak, hbm_peak, peak_kind),
-                            bench_prefill(args, 4, 32512, tc_peak, hbm_peak, peak_kind)]
+        extra = run_sections(args, hbm_peak, tc_peak, peak_kind)
     line = {
         "metric": "MoE-FFN decode tok/s (batch 1, one layer)",
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -446,8 +466,9 @@ def main():
     ap.add_argument("--replicas", type=int, default=8)
     ap.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--decode-only", action="store_true",
-                    help="time the decode workload only (no q=4 or prefill sections)")
+    ap.add_argument("--sections", default="decode,verify,prefill",
+                    help="comma list of decode, verify, prefill (= prefill3,prefill4); "
+                         "without decode only the named sections run (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

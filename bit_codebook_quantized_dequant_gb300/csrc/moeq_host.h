@@ -57,6 +57,32 @@ const DeviceInfo& device_info();
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOEQ_ERR_CUDA; }
 
+// One grouped GEMM of the prefill on the tensor cores (gemm_tc.cu): tiles of
+// 128 weight rows x 64 grouped rows over groups [g0, g1); gu = 1: gate and up
+// (wa, wb) with the SwiGLU + H32 + Q8 epilogue into hq / hd / hbf, gu = 0:
+// down (wa) into o. act: bf16 [rows x K] grouped activations (exact values of
+// the int8 codes), act_scale: their fp16 block scales [rows x K/32].
+struct TcGemm {
+  int gu;
+  DMat wa, wb;
+  int shared, g0, g1;
+  const int* toff;
+  const int* offsets;
+  int K, R, rows;
+  const uint16_t* act;
+  const uint16_t* act_scale;
+  int8_t* hq;
+  uint16_t* hd;
+  uint16_t* hbf;
+  const uint32_t* signs_h;
+  float* o;
+  const int* pid;
+  int T, k, ns;
+  moeq_debug dbg;
+  int32_t* status;
+};
+int tc_grouped_gemm(const TcGemm& g, cudaStream_t s);
+
 // Router + top-k of T tokens enqueued on s (route.cu).
 int route_topk_launch(const uint16_t* x, int T, const uint16_t* router, int E, int H, int k,
                       int32_t* idx, float* w, float* logits, cudaStream_t s);

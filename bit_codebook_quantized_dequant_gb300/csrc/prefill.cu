@@ -1,19 +1,16 @@
 // Expert-grouped prefill of T tokens: every token gets the decode's result
-// (up to fp32 rounding), computed as
+// (up to fp32 summation order), computed as
 //   router + top-k of every token              (route.cu)
 //   Q8 of every 32-block of x (after H32)       prep_x_kernel
 //   stable counting sort of the (token, slot) pairs by expert
 //                                               count_kernel, place_kernel
-//   grouped gate/up GEMM per expert, epilogue SwiGLU, H32 and Q8 of h
-//                                               gu_kernel
-//   grouped down GEMM per expert                down_kernel
+//   x's int8 codes as bf16 rows in grouped order gather_kernel
+//   grouped gate/up GEMM per expert on the tensor cores, epilogue SwiGLU,
+//   H32 and Q8 of h                             gemm_tc.cu
+//   grouped down GEMM per expert (tensor cores) gemm_tc.cu
 //   gather-combine in slot order (+ residual)   combine_kernel
 // all enqueued on the caller's stream with no host synchronization; the tile
 // lists of the grouped GEMMs are built on the device from the expert counts.
-//
-// The grouped GEMMs here run on the CUDA cores: a weight block is expanded
-// once per thread (byte permutes) and dotted (dp4a) with the int8 blocks of 8
-// tokens, with the per-block scales applied in fp32 as in the decode.
 //
 // Sources: "deepseek-v4-flash-0731-evox3-rocm", section "The optimization
 // ladder" (fused multi-token prefill, H32 on the activations); "Lucebox x
@@ -29,11 +26,8 @@
 namespace moeq {
 namespace {
 
-constexpr int kNT = 64;   // tokens (grouped rows) per GEMM tile
-constexpr int kMT = 32;   // weight rows per GEMM tile (one lane each)
-constexpr int kKB = 16;   // 32-blocks per K chunk staged in shared memory
-constexpr int kGemmThreads = 256;
-constexpr int kTokPerWarp = kNT / (kGemmThreads / 32);  // 8
+constexpr int kNT = 64;   // grouped rows per GEMM tile (gemm_tc.cu)
+constexpr int kMT = 128;  // weight rows per GEMM tile (gemm_tc.cu)
 
 struct PrefillArgs {
   int T, H, I, E, k, has_shared, ns;
@@ -51,8 +45,11 @@ struct PrefillArgs {
   int* tiles_dn;
   int* pid;
   int* pos;
+  uint16_t* xg;
+  uint16_t* xdg;
   int8_t* hq;
   uint16_t* hd;
+  uint16_t* hbf;
   float* o;
   const float* residual;
   float* y;
@@ -188,250 +185,41 @@ __global__ void place_kernel(const PrefillArgs a) {
   }
 }
 
-// Group of a tile from the tile offsets (binary search over groups [g0, g1)).
-__device__ __forceinline__ int tile_group(const int* toff, int g0, int g1, int tile) {
-  int lo = g0, hi = g1 - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&toff[mid]) <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ void pid_split(const PrefillArgs& a, int pid, int& t, int& s) {
+// Grouped activation rows for the tensor-core GEMM: row r of group order is
+// token t = the token of pid[r]; xg[r] = x's int8 codes of t as bf16 (exact),
+// xdg[r] = their fp16 block scales. One warp per grouped row.
+__global__ void gather_kernel(const PrefillArgs a, int rows) {
+  const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int pid = a.pid[r];
   const int Tk = a.T * a.k;
-  if (pid >= Tk) {
-    t = pid - Tk;
-    s = a.k;
-  } else {
-    t = pid / a.k;
-    s = pid - t * a.k;
-  }
-}
-
-template <int FMT>
-struct GemmSmem {
-  static constexpr int BC = block_bytes<FMT>();
-  static constexpr int WP = kKB * BC + 16;  // padded row pitch of a code tile
-  uint8_t w[2][kMT][WP];                    // codes of one or two matrices
-  uint16_t ws[2][kMT][kKB];                 // raw scales (fp16 bits or E8M0)
-  int8_t act[kNT][kKB * 32 + 16];           // int8 activations, one row per grouped row
-  float ad[kNT][kKB];                       // activation block scales
-  int tok[kNT];                             // activation row (token or grouped row), -1 = none
-  uint32_t cb[2][4];                        // codebook records
-};
-
-template <int FMT>
-__device__ __forceinline__ float raw_scale(uint16_t r) {
-  if constexpr (FMT == 4) return e8m0_to_f32(static_cast<uint8_t>(r));
-  else return f16_bits_to_f32(r);
-}
-
-// Stages K chunk [kc, kc + kb) of rows r0.. of NM matrices and of the tile's
-// activation rows into shared memory.
-template <int FMT, int NM>
-__device__ void stage_chunk(GemmSmem<FMT>& sm, const DMat* const* mats, int e, int r0, int K,
-                            int kc, int kb, const int8_t* act, int act_pitch, const uint16_t* adsc,
-                            int ad_pitch) {
-  constexpr int BC = block_bytes<FMT>();
-  const int nb = K / 32;
-  const int tid = threadIdx.x;
-  // codes: per row kb*BC bytes (a multiple of 8), in 8-byte pieces
-  const int pieces = kb * BC / 8;
-  for (int m = 0; m < NM; ++m) {
-    const DMat& M = *mats[m];
-    const uint8_t* base = M.codes + static_cast<size_t>(e) * M.stride_codes;
-    for (int i = tid; i < kMT * pieces; i += blockDim.x) {
-      const int r = i / pieces, c = i % pieces;
-      const uint2 v = *reinterpret_cast<const uint2*>(base + (static_cast<size_t>(r0 + r) * nb + kc) * BC + 8 * c);
-      *reinterpret_cast<uint2*>(&sm.w[m][r][8 * c]) = v;
-    }
-    const uint8_t* sb = M.scales + static_cast<size_t>(e) * M.stride_scales;
-    for (int i = tid; i < kMT * kb; i += blockDim.x) {
-      const int r = i / kb, c = i % kb;
-      const size_t at = static_cast<size_t>(r0 + r) * nb + kc + c;
-      sm.ws[m][r][c] = FMT == 4 ? static_cast<uint16_t>(sb[at]) : reinterpret_cast<const uint16_t*>(sb)[at];
-    }
-  }
-  // activations: kb*32 bytes per row in 16-byte pieces
-  const int ap = kb * 2;
-  for (int i = tid; i < kNT * ap; i += blockDim.x) {
-    const int j = i / ap, c = i % ap;
-    const int row = sm.tok[j];
-    int4 v = make_int4(0, 0, 0, 0);
-    if (row >= 0) v = *reinterpret_cast<const int4*>(act + static_cast<size_t>(row) * act_pitch + kc * 32 + 16 * c);
-    *reinterpret_cast<int4*>(&sm.act[j][16 * c]) = v;
-  }
-  for (int i = tid; i < kNT * kb; i += blockDim.x) {
-    const int j = i / kb, c = i % kb;
-    const int row = sm.tok[j];
-    sm.ad[j][c] = row >= 0 ? f16_bits_to_f32(adsc[static_cast<size_t>(row) * ad_pitch + kc + c]) : 0.0f;
-  }
-}
-
-__device__ __forceinline__ void load_q8(const int8_t* p, int* q) {
-  const int4 q0 = *reinterpret_cast<const int4*>(p);
-  const int4 q1 = *reinterpret_cast<const int4*>(p + 16);
-  q[0] = q0.x; q[1] = q0.y; q[2] = q0.z; q[3] = q0.w;
-  q[4] = q1.x; q[5] = q1.y; q[6] = q1.z; q[7] = q1.w;
-}
-
-// Grouped gate/up GEMM over the tiles of groups [g0, g1) with matrices G, U
-// (routed: expert = group; shared: expert 0). Tile = 32 rows of I x 64
-// grouped rows; epilogue: h = silu(g) u, then H32 + Q8 of the 32-block.
-template <int FMT>
-__global__ void __launch_bounds__(kGemmThreads) gu_kernel(const PrefillArgs a, int g0, int g1, int shared) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  GemmSmem<FMT>& sm = *reinterpret_cast<GemmSmem<FMT>*>(smem_raw);
-  constexpr int BC = block_bytes<FMT>();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const DMat& G = shared ? a.sgate : a.gate;
-  const DMat& U = shared ? a.sup : a.up;
-  const DMat* mats[2] = {&G, &U};
-  const int t_begin = a.tiles_gu[g0], t_end = a.tiles_gu[g1];
-  const int rtiles = a.I / kMT;
-  const int nb = a.H / 32;
-  for (int tile = t_begin + blockIdx.x; tile < t_end; tile += gridDim.x) {
-    const int g = tile_group(a.tiles_gu, g0, g1, tile);
-    const int local = tile - a.tiles_gu[g];
-    const int tt = local / rtiles, rt = local % rtiles;
-    const int off = a.offsets[g], n = a.offsets[g + 1] - off;
-    const int e = shared ? 0 : g;
-    const int i0 = rt * kMT;
-    __syncthreads();  // the previous tile's shared memory is free
-    if (threadIdx.x < kNT) {
-      const int j = tt * kNT + threadIdx.x;
-      int row = -1;
-      if (j < n) {
-        int t, s;
-        pid_split(a, a.pid[off + j], t, s);
-        row = t;
-      }
-      sm.tok[threadIdx.x] = row;
-    }
-    if (threadIdx.x < 8) {
-      const DMat& M = threadIdx.x < 4 ? G : U;
-      sm.cb[threadIdx.x / 4][threadIdx.x % 4] =
-          reinterpret_cast<const uint32_t*>(M.cb + static_cast<size_t>(e) * M.cb_stride)[threadIdx.x % 4];
-    }
-    __syncthreads();
-    float ag[kTokPerWarp], au[kTokPerWarp];
+  const int t = pid >= Tk ? pid - Tk : pid / a.k;
+  const int nbH = a.H / 32;
+  const int8_t* src = a.xq + static_cast<size_t>(t) * a.H;
+  uint16_t* dst = a.xg + static_cast<size_t>(r) * a.H;
+  for (int c = lane; c < a.H / 16; c += 32) {  // 16 codes per step
+    const int4 q = *reinterpret_cast<const int4*>(src + 16 * c);
+    const uint32_t w[4] = {static_cast<uint32_t>(q.x), static_cast<uint32_t>(q.y), static_cast<uint32_t>(q.z),
+                           static_cast<uint32_t>(q.w)};
+    uint32_t o[8];
 #pragma unroll
-    for (int t = 0; t < kTokPerWarp; ++t) ag[t] = au[t] = 0.0f;
-    for (int kc = 0; kc < nb; kc += kKB) {
-      const int kb = min(kKB, nb - kc);
-      stage_chunk<FMT, 2>(sm, mats, e, i0, a.H, kc, kb, a.xq, a.H, a.xd, nb);
-      __syncthreads();
-      const uint32_t* cbg = sm.cb[0];
-      const uint32_t* cbu = sm.cb[1];
-#pragma unroll 1
-      for (int b = 0; b < kb; ++b) {
-        uint32_t vg[8], vu[8];
-        block_expand<FMT>(&sm.w[0][lane][b * BC], cbg, vg);
-        block_expand<FMT>(&sm.w[1][lane][b * BC], cbu, vu);
-        const float wsg = raw_scale<FMT>(sm.ws[0][lane][b]);
-        const float wsu = raw_scale<FMT>(sm.ws[1][lane][b]);
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-        for (int t = 0; t < kTokPerWarp; ++t) {
-          const int j = warp * kTokPerWarp + t;
-          int q[8];
-          load_q8(&sm.act[j][32 * b], q);
-          const float d = sm.ad[j][b];
-          ag[t] = fmaf(wsg * d, static_cast<float>(dot8(vg, q)), ag[t]);
-          au[t] = fmaf(wsu * d, static_cast<float>(dot8(vu, q)), au[t]);
-        }
-      }
-      __syncthreads();
-    }
-    // epilogue: lane = row i0 + lane of I, one 32-block of h per token
-#pragma unroll 1
-    for (int t = 0; t < kTokPerWarp; ++t) {
-      const int j = tt * kNT + warp * kTokPerWarp + t;
-      if (j >= n) break;  // warp-uniform
-      const float h = ag[t] * au[t] / (1.0f + expf(-ag[t]));
-      float v = h;
-      if (a.signs_h) v = h32_warp(v, __ldg(&a.signs_h[i0 / 32]), lane);
-      uint16_t db;
-      const int8_t q = q8_warp(v, db);
-      const size_t row = static_cast<size_t>(off + j);
-      a.hq[row * a.I + i0 + lane] = q;
-      if (lane == 0) a.hd[row * (a.I / 32) + i0 / 32] = db;
-      if (a.dbg.h || a.dbg.hq || a.dbg.hd) {
-        int tk, s;
-        pid_split(a, a.pid[off + j], tk, s);
-        const size_t vec = static_cast<size_t>(tk) * a.ns + s;
-        if (a.dbg.h) a.dbg.h[vec * a.I + i0 + lane] = h;
-        if (a.dbg.hq) a.dbg.hq[vec * a.I + i0 + lane] = q;
-        if (a.dbg.hd && lane == 0) a.dbg.hd[vec * (a.I / 32) + i0 / 32] = db;
+      for (int h = 0; h < 2; ++h) {
+        const int v0 = static_cast<int8_t>(w[i] >> (16 * h));
+        const int v1 = static_cast<int8_t>(w[i] >> (16 * h + 8));
+        const uint32_t b0 = __float_as_uint(static_cast<float>(v0)) >> 16;
+        const uint32_t b1 = __float_as_uint(static_cast<float>(v1)) >> 16;
+        o[2 * i + h] = b0 | (b1 << 16);
       }
     }
+    uint4* d = reinterpret_cast<uint4*>(dst + 16 * c);
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
-}
-
-// Grouped down GEMM: o[row, :] = W_down[e] hq[row] over the tiles of groups
-// [g0, g1). Tile = 32 rows of H x 64 grouped rows.
-template <int FMT>
-__global__ void __launch_bounds__(kGemmThreads) down_kernel(const PrefillArgs a, int g0, int g1, int shared) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  GemmSmem<FMT>& sm = *reinterpret_cast<GemmSmem<FMT>*>(smem_raw);
-  constexpr int BC = block_bytes<FMT>();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const DMat& D = shared ? a.sdown : a.down;
-  const DMat* mats[1] = {&D};
-  const int t_begin = a.tiles_dn[g0], t_end = a.tiles_dn[g1];
-  const int rtiles = a.H / kMT;
-  const int nb = a.I / 32;
-  for (int tile = t_begin + blockIdx.x; tile < t_end; tile += gridDim.x) {
-    const int g = tile_group(a.tiles_dn, g0, g1, tile);
-    const int local = tile - a.tiles_dn[g];
-    const int tt = local / rtiles, rt = local % rtiles;
-    const int off = a.offsets[g], n = a.offsets[g + 1] - off;
-    const int e = shared ? 0 : g;
-    const int r0 = rt * kMT;
-    __syncthreads();
-    if (threadIdx.x < kNT) {
-      const int j = tt * kNT + threadIdx.x;
-      sm.tok[threadIdx.x] = j < n ? off + j : -1;  // activation rows are grouped rows
-    }
-    if (threadIdx.x < 4)
-      sm.cb[0][threadIdx.x] = reinterpret_cast<const uint32_t*>(D.cb + static_cast<size_t>(e) * D.cb_stride)[threadIdx.x];
-    __syncthreads();
-    float acc[kTokPerWarp];
-#pragma unroll
-    for (int t = 0; t < kTokPerWarp; ++t) acc[t] = 0.0f;
-    for (int kc = 0; kc < nb; kc += kKB) {
-      const int kb = min(kKB, nb - kc);
-      stage_chunk<FMT, 1>(sm, mats, e, r0, a.I, kc, kb, a.hq, a.I, a.hd, nb);
-      __syncthreads();
-#pragma unroll 1
-      for (int b = 0; b < kb; ++b) {
-        uint32_t v[8];
-        block_expand<FMT>(&sm.w[0][lane][b * BC], sm.cb[0], v);
-        const float ws = raw_scale<FMT>(sm.ws[0][lane][b]);
-#pragma unroll
-        for (int t = 0; t < kTokPerWarp; ++t) {
-          const int j = warp * kTokPerWarp + t;
-          int q[8];
-          load_q8(&sm.act[j][32 * b], q);
-          acc[t] = fmaf(ws * sm.ad[j][b], static_cast<float>(dot8(v, q)), acc[t]);
-        }
-      }
-      __syncthreads();
-    }
-#pragma unroll 1
-    for (int t = 0; t < kTokPerWarp; ++t) {
-      const int j = tt * kNT + warp * kTokPerWarp + t;
-      if (j >= n) break;
-      const size_t row = static_cast<size_t>(off + j);
-      a.o[row * a.H + r0 + lane] = acc[t];
-      if (a.dbg.o) {
-        int tk, s;
-        pid_split(a, a.pid[off + j], tk, s);
-        a.dbg.o[(static_cast<size_t>(tk) * a.ns + s) * a.H + r0 + lane] = acc[t];
-      }
-    }
-  }
+  for (int b = lane; b < nbH; b += 32)
+    a.xdg[static_cast<size_t>(r) * nbH + b] = a.xd[static_cast<size_t>(t) * nbH + b];
 }
 
 // y[t, :] = sum_s p[t, s] o[pos[t, s], :] (+ o_shared[t, :]) (+ residual[t, :]),
@@ -467,36 +255,6 @@ __global__ void combine_kernel(const PrefillArgs a) {
 __global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ x, float* __restrict__ r, size_t n) {
   const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < n) r[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
-}
-
-template <int FMT>
-int launch_gu(const PrefillArgs& a, int g0, int g1, int shared, int grid, cudaStream_t s) {
-  const int smem = static_cast<int>(sizeof(GemmSmem<FMT>));
-  if (cudaFuncSetAttribute(gu_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return MOEQ_ERR_CUDA;
-  gu_kernel<FMT><<<grid, kGemmThreads, smem, s>>>(a, g0, g1, shared);
-  return cuda_status(cudaGetLastError());
-}
-
-template <int FMT>
-int launch_down(const PrefillArgs& a, int g0, int g1, int shared, int grid, cudaStream_t s) {
-  const int smem = static_cast<int>(sizeof(GemmSmem<FMT>));
-  if (cudaFuncSetAttribute(down_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return MOEQ_ERR_CUDA;
-  down_kernel<FMT><<<grid, kGemmThreads, smem, s>>>(a, g0, g1, shared);
-  return cuda_status(cudaGetLastError());
-}
-
-int gu_any(int fmt, const PrefillArgs& a, int g0, int g1, int shared, int grid, cudaStream_t s) {
-  if (fmt == 2) return launch_gu<2>(a, g0, g1, shared, grid, s);
-  if (fmt == 3) return launch_gu<3>(a, g0, g1, shared, grid, s);
-  return launch_gu<4>(a, g0, g1, shared, grid, s);
-}
-
-int down_any(int fmt, const PrefillArgs& a, int g0, int g1, int shared, int grid, cudaStream_t s) {
-  if (fmt == 2) return launch_down<2>(a, g0, g1, shared, grid, s);
-  if (fmt == 3) return launch_down<3>(a, g0, g1, shared, grid, s);
-  return launch_down<4>(a, g0, g1, shared, grid, s);
 }
 
 }  // namespace
@@ -540,8 +298,11 @@ extern "C" int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, co
   a.tiles_dn = reinterpret_cast<int*>(w + wl.tiles_dn);
   a.pid = reinterpret_cast<int*>(w + wl.pid);
   a.pos = reinterpret_cast<int*>(w + wl.pos);
+  a.xg = reinterpret_cast<uint16_t*>(w + wl.xg);
+  a.xdg = reinterpret_cast<uint16_t*>(w + wl.xdg);
   a.hq = reinterpret_cast<int8_t*>(w + wl.hq);
   a.hd = reinterpret_cast<uint16_t*>(w + wl.hd);
+  a.hbf = reinterpret_cast<uint16_t*>(w + wl.hbf);
   a.o = reinterpret_cast<float*>(w + wl.o);
   a.residual = residual;
   a.y = y;
@@ -565,11 +326,49 @@ extern "C" int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, co
     if (dbg->p && (rc = cuda_status(cudaMemcpyAsync(dbg->p, a.p, 4 * tk, cudaMemcpyDeviceToDevice, s))))
       return rc;
   }
-  const int grid = device_info().sm_count * 3;
-  if ((rc = gu_any(L->gate.fmt, a, 0, L->E, 0, grid, s))) return rc;
-  if (a.has_shared && (rc = gu_any(L->sgate.fmt, a, L->E, L->E + 1, 1, grid, s))) return rc;
-  if ((rc = down_any(L->down.fmt, a, 0, L->E, 0, grid, s))) return rc;
-  if (a.has_shared && (rc = down_any(L->sdown.fmt, a, L->E, L->E + 1, 1, grid, s))) return rc;
+  const int rows = T * L->k + (a.has_shared ? T : 0);
+  gather_kernel<<<(rows + 7) / 8, 256, 0, s>>>(a, rows);
+  if ((rc = cuda_status(cudaGetLastError()))) return rc;
+  TcGemm g{};
+  g.offsets = a.offsets;
+  g.rows = rows;
+  g.hq = a.hq;
+  g.hd = a.hd;
+  g.hbf = a.hbf;
+  g.signs_h = a.signs_h;
+  g.o = a.o;
+  g.pid = a.pid;
+  g.T = T;
+  g.k = L->k;
+  g.ns = a.ns;
+  g.dbg = a.dbg;
+  g.status = dev_status;
+  for (int pass = 0; pass < 4; ++pass) {
+    const bool gu = pass < 2, shared = pass & 1;
+    if (shared && !a.has_shared) continue;
+    g.gu = gu ? 1 : 0;
+    g.shared = shared ? 1 : 0;
+    g.g0 = shared ? L->E : 0;
+    g.g1 = shared ? L->E + 1 : L->E;
+    if (gu) {
+      g.wa = shared ? a.sgate : a.gate;
+      g.wb = shared ? a.sup : a.up;
+      g.toff = a.tiles_gu;
+      g.K = L->H;
+      g.R = L->I;
+      g.act = a.xg;
+      g.act_scale = a.xdg;
+    } else {
+      g.wa = shared ? a.sdown : a.down;
+      g.wb = g.wa;
+      g.toff = a.tiles_dn;
+      g.K = L->I;
+      g.R = L->H;
+      g.act = a.hbf;
+      g.act_scale = a.hd;
+    }
+    if ((rc = tc_grouped_gemm(g, s))) return rc;
+  }
   const size_t nout = static_cast<size_t>(T) * (L->H / 4);
   combine_kernel<<<static_cast<unsigned>((nout + 255) / 256), 256, 0, s>>>(a);
   return cuda_status(cudaGetLastError());
