@@ -47,6 +47,8 @@ constexpr int kKC = 8;         // 32-blocks per raw code chunk
 constexpr int kSlots = 3;      // operand slots (2 blocks each)
 constexpr int kBufs = 4;       // TMEM accumulator buffers (1 block each)
 constexpr int kScs = 6;        // scale slots (2 blocks each)
+constexpr int kXd = 4;         // pairs the activation scales are fetched ahead
+constexpr int kXr = 8;         // their staging ring (> kXd)
 constexpr int kTcThreads = 512;
 constexpr int kBWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -56,15 +58,19 @@ constexpr uint32_t kTmemCols = 512;
 template <int FMT>
 struct TcSmem {
   static constexpr int BC = block_bytes<FMT>();
-  static constexpr int RP = kKC * BC + 16;  // raw row pitch (16 B of padding against bank conflicts)
+  // raw row: the chunk's codes, then its block scales (<= 16 B); the pitch
+  // also keeps the rows of a warp on different banks
+  static constexpr int RP = kKC * BC + 16;
   uint8_t a[kSlots][2][kTM * 128];          // A operand: 128 rows x 64 bf16, SW128 K-major
   uint8_t b[kSlots][kTN * 128];             // B operand: 64 rows x 64 bf16, SW128 K-major
   uint8_t raw[2][2][kTM][RP];               // packed code chunks [stage][matrix][row]
   float ws[kScs][2][2][kTM];                // weight block scales [slot][block][matrix][row]
   float xd[kScs][2][kTN];                   // activation block scales [slot][block][row]
+  uint32_t xraw[kXr][kTN];                  // fp16 pairs of activation scales, kXd pairs ahead
   uint64_t ab_full[kSlots], ab_empty[kSlots];
   uint64_t acc_full[kBufs], acc_empty[kBufs];
   uint64_t sc_full[kScs], sc_empty[kScs];
+  uint64_t drain;                           // completion of every MMA this CTA issued
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -122,6 +128,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Packed fp32 pairs (each lane an IEEE fp32 operation, round to nearest).
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -134,15 +160,34 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
 }
+// 4- or 8-byte asynchronous copies (cache-all variant); src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" :: "r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
-// Bounded wait on an mbarrier phase by one lane, observing the abort flag.
+// mbarrier phase test that lets the hardware suspend the thread (up to 1 us)
+// until the phase completes, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
+               "selp.u32 %0, 1, 0, p;\n}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase by one lane, observing the abort flag
+// (at most kSpinLimit suspensions of at most 1 us).
 template <int FMT>
 __device__ __forceinline__ bool ring_wait(TcSmem<FMT>& sm, uint64_t* bar, uint32_t parity, int32_t* status) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (sm.abort) return false;
   }
   sm.abort = 1;
@@ -220,13 +265,6 @@ __device__ __forceinline__ void expand_bf16(const uint8_t* p, const uint32_t* tl
   }
 }
 
-template <int FMT>
-__device__ __forceinline__ float wscale(const DMat& M, int e, size_t at) {
-  const uint8_t* s = M.scales + static_cast<size_t>(e) * M.stride_scales;
-  if constexpr (FMT == 4) return e8m0_to_f32(s[at]);
-  else return f16_bits_to_f32(reinterpret_cast<const uint16_t*>(s)[at]);
-}
-
 struct TileInfo {
   int g, e, m0, tt, off, n;
 };
@@ -261,6 +299,19 @@ __device__ __forceinline__ void pid_split(const TcArgs& a, int pid, int& t, int&
   }
 }
 
+// Timeline event of CTA 0 (debug only): role 0 expansion, 1 producer, 2 MMA,
+// 3 epilogue; (globaltimer ns, event << 32 | counter).
+__device__ __forceinline__ void tc_trace(const TcArgs& a, int role, int& n, uint32_t ev, int ctr) {
+  if (a.dbg.trace && blockIdx.x == 0 && n < a.dbg.trace_cap) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    uint64_t* p = a.dbg.trace + 2 * (static_cast<size_t>(role) * a.dbg.trace_cap + n);
+    p[0] = t;
+    p[1] = (static_cast<uint64_t>(ev) << 32) | static_cast<uint32_t>(ctr);
+  }
+  ++n;
+}
+
 // ---------------------------------------------------------------- kernel
 template <int FMT, bool GU>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
@@ -289,6 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       mbar_init(&sm.sc_full[i], 5);
       mbar_init(&sm.sc_empty[i], 8);
     }
+    mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -305,26 +357,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   if (warp < 4) {
     // ------------------------------------------------------------ expansion (thread = row)
     const int r = tid;
-    int ks = 0;
+    int ks = 0, ntr = 0;
     for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
       const TileInfo t = tile_info(a, t_begin + ti);
-      const DMat* mats[2] = {&a.wa, &a.wb};
       uint32_t tl[2][4], th[2][4];
 #pragma unroll
       for (int m = 0; m < NM; ++m) {
-        const DMat& M = *mats[m];
+        const DMat& M = m == 0 ? a.wa : a.wb;
         cb_tables(M.cb + static_cast<size_t>(t.e) * M.cb_stride, 1 << FMT, tl[m], th[m]);
       }
       const size_t row = static_cast<size_t>(t.m0 + r);
+      // one chunk of the row: its codes and its block scales, by asynchronous copies
       auto issue_chunk = [&](int c) {
+        constexpr int SB = FMT == 4 ? 1 : 2;
         const int kc = c * kKC, kb = min(kKC, nb - kc);
         const int pieces = kb * BC / 16;
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
-          const DMat& M = *mats[m];
+          const DMat& M = m == 0 ? a.wa : a.wb;
           const uint8_t* src = M.codes + static_cast<size_t>(t.e) * M.stride_codes + (row * nb + kc) * BC;
           uint8_t* dst = sm.raw[c & 1][m][r];
           for (int i = 0; i < pieces; ++i) cp_async16(dst + 16 * i, src + 16 * i);
+          const size_t soff = (row * nb + kc) * SB;
+          const uint8_t* ssrc = M.scales + static_cast<size_t>(t.e) * M.stride_scales + soff;
+          uint8_t* sdst = dst + kKC * BC;
+          const int sbytes = kb * SB;  // 4, 8 or 16; soff is aligned to the piece used
+          if (sbytes % 16 == 0 && soff % 16 == 0) {
+            for (int i = 0; i < sbytes; i += 16) cp_async16(sdst + i, ssrc + i);
+          } else if (sbytes % 8 == 0 && soff % 8 == 0) {
+            for (int i = 0; i < sbytes; i += 8) cp_async8(sdst + i, ssrc + i);
+          } else {
+            for (int i = 0; i < sbytes; i += 4) cp_async4(sdst + i, ssrc + i, 4);
+          }
         }
         cp_async_commit();
       };
@@ -337,15 +401,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         } else {
           cp_async_wait<0>();
         }
+        if (tid == 0) tc_trace(a, 0, ntr, 4, c);
         const int kc = c * kKC, kb = min(kKC, nb - kc);
         for (int jp = 0; jp < kb / 2; ++jp, ++ks) {
           const int slot = ks % kSlots, scs = ks % kScs;
+          if (tid == 0) tc_trace(a, 0, ntr, 1, ks);
           if (ks >= kSlots && !warp_wait<FMT>(sm, &sm.ab_empty[slot], ((ks / kSlots) - 1) & 1, a.status, lane)) break;
-          float wsr[NM][2];  // the row's block scales, loaded before the expansion hides their latency
+          if (tid == 0) tc_trace(a, 0, ntr, 2, ks);
+          float wsr[NM][2];
 #pragma unroll
           for (int m = 0; m < NM; ++m)
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) wsr[m][hb] = wscale<FMT>(*mats[m], t.e, row * nb + kc + 2 * jp + hb);
+            for (int hb = 0; hb < 2; ++hb) {
+              const uint8_t* sp = &sm.raw[c & 1][m][r][kKC * BC];
+              if constexpr (FMT == 4) wsr[m][hb] = e8m0_to_f32(sp[2 * jp + hb]);
+              else wsr[m][hb] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(sp)[2 * jp + hb]);
+            }
 #pragma unroll
           for (int m = 0; m < NM; ++m) {
 #pragma unroll
@@ -360,6 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
               }
             }
           }
+          if (tid == 0) tc_trace(a, 0, ntr, 3, ks);
           if (ks >= kScs && !warp_wait<FMT>(sm, &sm.sc_empty[scs], ((ks / kScs) - 1) & 1, a.status, lane)) break;
 #pragma unroll
           for (int m = 0; m < NM; ++m)
@@ -378,40 +450,59 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     cp_async_wait<0>();
   } else if (warp == kBWarp) {
     // ------------------------------------------------------------ activation producer
-    int ks = 0;
+    int ks = 0, ntr = 0;
     for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
       const TileInfo t = tile_info(a, t_begin + ti);
       const int y0 = t.off + t.tt * kTN;
+      // the 2 fp16 scales of a pair for rows lane and lane + 32, kXd pairs ahead
+      // (one copy group per pair; a lane only reads what it copied)
+      auto fetch_xd = [&](int p) {
+        if (p < npairs) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = lane + 32 * h, jr = t.tt * kTN + j;
+            const uint16_t* src = a.act_scale + static_cast<size_t>(t.off + (jr < t.n ? jr : 0)) * nb + 2 * p;
+            cp_async4(&sm.xraw[p % kXr][j], src, jr < t.n ? 4u : 0u);
+          }
+        }
+        cp_async_commit();
+      };
+      for (int p = 0; p < kXd; ++p) fetch_xd(p);
       for (int p = 0; p < npairs; ++p, ++ks) {
         const int slot = ks % kSlots, scs = ks % kScs;
         if (ks >= kSlots && !warp_wait<FMT>(sm, &sm.ab_empty[slot], ((ks / kSlots) - 1) & 1, a.status, lane)) break;
+        if (lane == 0) tc_trace(a, 1, ntr, 2, ks);
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.ab_full[slot], kTN * 128);
           tma_load_2d(sm.b[slot], &tm_act, 64 * p, y0, &sm.ab_full[slot]);
         }
         if (ks >= kScs && !warp_wait<FMT>(sm, &sm.sc_empty[scs], ((ks / kScs) - 1) & 1, a.status, lane)) break;
+        fetch_xd(p + kXd);
+        cp_async_wait<kXd>();  // this pair's group has landed
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int j = lane + 32 * h;
-          const int jr = t.tt * kTN + j;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-            sm.xd[scs][hb][j] =
-                jr < t.n ? f16_bits_to_f32(a.act_scale[static_cast<size_t>(t.off + jr) * nb + 2 * p + hb]) : 0.0f;
+          const uint32_t v = sm.xraw[p % kXr][lane + 32 * h];
+          sm.xd[scs][0][lane + 32 * h] = f16_bits_to_f32(static_cast<uint16_t>(v & 0xffffu));
+          sm.xd[scs][1][lane + 32 * h] = f16_bits_to_f32(static_cast<uint16_t>(v >> 16));
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.sc_full[scs]);
+        if (lane == 0) {
+          mbar_arrive(&sm.sc_full[scs]);
+          tc_trace(a, 1, ntr, 5, ks);
+        }
       }
+      cp_async_wait<0>();
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
-      int ks = 0, kg = 0;
+      int ks = 0, kg = 0, ntr = 0;
       bool ok = true;
       for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
         for (int p = 0; p < npairs && ok; ++p, ++ks) {
           const int slot = ks % kSlots;
           if (!(ok = ring_wait<FMT>(sm, &sm.ab_full[slot], (ks / kSlots) & 1, a.status))) break;
+          tc_trace(a, 2, ntr, 2, ks);
           tc_fence_after();
           const uint32_t abase[2] = {smem_u32(sm.a[slot][0]), smem_u32(sm.a[slot][1])};
           const uint32_t bbase = smem_u32(sm.b[slot]);
@@ -420,6 +511,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             const int buf = kg % kBufs;
             if (kg >= kBufs && !(ok = ring_wait<FMT>(sm, &sm.acc_empty[buf], ((kg / kBufs) - 1) & 1, a.status)))
               break;
+            tc_trace(a, 2, ntr, 6, kg);
             tc_fence_after();
             const uint32_t dcol = tmem + static_cast<uint32_t>(buf * (GU ? 2 * kTN : kTN));
 #pragma unroll
@@ -436,6 +528,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
           if (ok) mma_commit(&sm.ab_empty[slot]);
         }
       }
+      // TMEM is released only after every MMA this thread issued has completed
+      // (also when a wait above ran out and the loops were left early)
+      mma_commit(&sm.drain);
+      bool drained = false;
+      for (uint32_t i = 0; i < kSpinLimit && !drained; ++i) drained = mbar_try_wait_sleep(&sm.drain, 0);
+      if (!drained) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
@@ -444,15 +542,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     const int half = (warp - kEpiWarp0) >> 2;
     const int c0 = 32 * half;         // this warpgroup's 32 columns
     const int r = 32 * q + lane;
-    int ks = 0, kg = 0;
+    int ks = 0, kg = 0, ntr = 0;
     bool ok = true;
     for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
       const TileInfo t = tile_info(a, t_begin + ti);
-      float acc[NM][32];
+      uint64_t acc[NM][16];  // column pairs (2j, 2j + 1) of this warpgroup's 32 columns
 #pragma unroll
       for (int m = 0; m < NM; ++m)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[m][j] = 0.0f;
+        for (int j = 0; j < 16; ++j) acc[m][j] = 0ull;
       for (int p = 0; p < npairs && ok; ++p, ++ks) {
         const int scs = ks % kScs;
         if (!(ok = warp_wait<FMT>(sm, &sm.sc_full[scs], (ks / kScs) & 1, a.status, lane))) break;
@@ -460,37 +558,57 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         for (int hb = 0; hb < 2; ++hb, ++kg) {
           const int buf = kg % kBufs;
           if (!(ok = warp_wait<FMT>(sm, &sm.acc_full[buf], (kg / kBufs) & 1, a.status, lane))) break;
+          if (tid == 32 * kEpiWarp0) tc_trace(a, 3, ntr, 6, kg);
           tc_fence_after();
+          const float4* xdv = reinterpret_cast<const float4*>(&sm.xd[scs][hb][c0]);
 #pragma unroll
           for (int m = 0; m < NM; ++m) {
             const float wsv = sm.ws[scs][hb][m][r];
+            const uint64_t ws2 = pack2(wsv, wsv);
+            const uint32_t col = static_cast<uint32_t>(buf * (GU ? 2 * kTN : kTN) + m * kTN + c0);
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col;
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
               float S[16];
-              const uint32_t col = static_cast<uint32_t>(buf * (GU ? 2 * kTN : kTN) + m * kTN + c0 + 16 * ch);
-              tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, S);
+              tmem_ld16(taddr + 16 * ch, S);
               tmem_wait_ld();
+              // acc = fma(ws * xd, S, acc) per column, two columns per instruction
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                acc[m][16 * ch + j] = fmaf(wsv * sm.xd[scs][hb][c0 + 16 * ch + j], S[j], acc[m][16 * ch + j]);
+              for (int i = 0; i < 4; ++i) {
+                const float4 x4 = xdv[4 * ch + i];
+                const uint64_t sc0 = mul2(ws2, pack2(x4.x, x4.y));
+                const uint64_t sc1 = mul2(ws2, pack2(x4.z, x4.w));
+                acc[m][8 * ch + 2 * i] = fma2(sc0, pack2(S[4 * i], S[4 * i + 1]), acc[m][8 * ch + 2 * i]);
+                acc[m][8 * ch + 2 * i + 1] = fma2(sc1, pack2(S[4 * i + 2], S[4 * i + 3]), acc[m][8 * ch + 2 * i + 1]);
+              }
             }
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+          if (tid == 32 * kEpiWarp0) tc_trace(a, 3, ntr, 7, kg);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.sc_empty[scs]);
       }
       if (!ok) break;
-      // tile epilogue: 32 columns of this warpgroup; row m0 + r
-#pragma unroll 1
+      if (tid == 32 * kEpiWarp0) tc_trace(a, 3, ntr, 8, ti);
+      // tile epilogue: 32 columns of this warpgroup; row m0 + r (unrolled:
+      // the accumulators stay in registers)
+#pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int jr = t.tt * kTN + c0 + j;
-        if (jr >= t.n) break;  // warp-uniform
+        if (jr >= t.n) continue;  // warp-uniform
         const size_t grow = static_cast<size_t>(t.off + jr);
+        float av[NM];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          float lo, hi;
+          unpack2(acc[m][j / 2], lo, hi);
+          av[m] = (j & 1) ? hi : lo;
+        }
         if constexpr (GU) {
-          const float g = acc[0][j], u = acc[1][j];
+          const float g = av[0], u = av[NM - 1];
           const float h = g * u / (1.0f + expf(-g));
           const int blk = (t.m0 + 32 * q) / 32;
           float v = h;
@@ -510,11 +628,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             if (a.dbg.hd && lane == 0) a.dbg.hd[vec * (a.R / 32) + blk] = db;
           }
         } else {
-          a.o[grow * a.R + t.m0 + r] = acc[0][j];
+          a.o[grow * a.R + t.m0 + r] = av[0];
           if (a.dbg.o) {
             int tk, s;
             pid_split(a, a.pid[grow], tk, s);
-            a.dbg.o[(static_cast<size_t>(tk) * a.ns + s) * a.R + t.m0 + r] = acc[0][j];
+            a.dbg.o[(static_cast<size_t>(tk) * a.ns + s) * a.R + t.m0 + r] = av[0];
           }
         }
       }

@@ -367,6 +367,7 @@ extern "C" int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, co
       g.act = a.hbf;
       g.act_scale = a.hd;
     }
+    g.dbg.trace = pass == 0 ? a.dbg.trace : nullptr;  // the timeline covers the routed gate/up GEMM
     if ((rc = tc_grouped_gemm(g, s))) return rc;
   }
   const size_t nout = static_cast<size_t>(T) * (L->H / 4);

@@ -102,7 +102,10 @@ typedef struct {
   int32_t* S_gate, *S_up;       /* decode / q=4: [T x slots x I x H/32] int32 block partials */
   int32_t* S_down;              /* decode / q=4: [T x slots x H x I/32] */
   uint64_t* trace;              /* decode / q=4: timeline, [grid x 4 roles x trace_cap x 2]
-                                   of (globaltimer ns, event << 32 | unit); see MOEQ_TRACE_* */
+                                   of (globaltimer ns, event << 32 | unit), see MOEQ_TRACE_*;
+                                   prefill: CTA 0 of the routed gate/up GEMM, [4 roles x
+                                   trace_cap x 2] (roles: expansion, activation producer,
+                                   MMA issue, epilogue) */
   int trace_cap;                /* events per (CTA, role) */
 } moeq_debug;
 
