@@ -1,6 +1,7 @@
 // Host-side parts of the C ABI: sizes, descriptor validation, workspace helpers.
 #include <cuda_runtime.h>
 
+#include <deque>
 #include <mutex>
 #include <vector>
 
@@ -55,7 +56,7 @@ int validate_layer(const moeq_layer* L) {
 
 const DeviceInfo& device_info() {
   static std::mutex mu;
-  static std::vector<DeviceInfo> cache;
+  static std::deque<DeviceInfo> cache;  // references stay valid as devices are added
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lk(mu);
