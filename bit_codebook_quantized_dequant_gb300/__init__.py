@@ -88,6 +88,7 @@ def _declare(L):
         "moe_pack_expert": (i, [i, i, i, P, P, P, P, P, P]),
         "moe_route_topk": (i, [P, i, P, i, i, i, P, P, P, P, P]),
         "moe_ffn_decode": (i, [C.POINTER(MoeqLayer), P, P, P, sz, P, C.POINTER(MoeqDebug), P]),
+        "moe_ffn_decode_static": (i, [C.POINTER(MoeqLayer), P, P, P, P]),
         "moe_ffn_verify_q4": (i, [C.POINTER(MoeqLayer), C.POINTER(MoeqMatrix), P, P, P, P, sz, P,
                                   C.POINTER(MoeqDebug), P]),
         "moe_ffn_prefill": (i, [C.POINTER(MoeqLayer), P, i, P, P, P, sz, P, C.POINTER(MoeqDebug),
@@ -107,6 +108,7 @@ def _declare(L):
 
 EXPORTED = ["moeq_packed_bytes", "moeq_validate_layer", "moe_ffn_workspace",
             "moe_ffn_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_ffn_decode",
+            "moe_ffn_decode_static",
             "moe_ffn_verify_q4", "moe_ffn_prefill", "moe_ffn_stack_prefill", "h32_rotate",
             "moe_rmsnorm_bf16",
             "moeq_version", "moeq_synth_codes", "moeq_synth_scales"]
@@ -171,6 +173,12 @@ def moe_ffn_decode(layer: MoeqLayer, x, y, ws, ws_bytes, dev_status=None, dbg=No
     return _check("moe_ffn_decode", load().moe_ffn_decode(
         C.byref(layer), _ptr(x), _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status),
         C.byref(dbg) if dbg is not None else None, _stream(stream)))
+
+
+def moe_ffn_decode_static(layer: MoeqLayer, x, y, dev_status=None, stream=None):
+    """moe_ffn_decode with the library's own per-device scratch (no workspace)."""
+    return _check("moe_ffn_decode_static", load().moe_ffn_decode_static(
+        C.byref(layer), _ptr(x), _ptr(y), _ptr(dev_status), _stream(stream)))
 
 
 def moe_ffn_verify_q4(layer: MoeqLayer, dense, x, y, y_dense, ws, ws_bytes, dev_status=None,

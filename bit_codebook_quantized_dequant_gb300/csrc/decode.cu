@@ -51,6 +51,8 @@
 // Geometric" (fused matvec, sync-free MoE decode).
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "moeq.h"
 #include "moeq_device.cuh"
 #include "moeq_host.h"
@@ -1312,4 +1314,55 @@ extern "C" int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, 
     a.nDN = dense->rows / kDownRows;
   }
   return launch<4>(a, dbg != nullptr, stream);
+}
+
+// ---------------------------------------------------------------- decode with library-owned scratch
+// The decode's scratch (counters, routing record, logits, quantized h,
+// per-expert outputs) lives here instead of in a caller workspace, for
+// callers that cannot allocate device memory. One array per device (the
+// module's copy on each device); its address is looked up once per device.
+namespace moeq {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 160 * 1024;  // decode shapes up to this workspace size
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices];
+
+// Address of this device's scratch (the current device), or nullptr.
+void* static_scratch(int device) {
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+    g_scratch_ptr[device] = p;
+  }
+  return g_scratch_ptr[device];
+}
+
+}  // namespace
+}  // namespace moeq
+
+extern "C" int moe_ffn_decode_static(const moeq_layer* L, const uint16_t* x, float* y, int32_t* dev_status,
+                                     moeq_stream stream) {
+  int rc = validate_layer(L);
+  if (rc) return rc;
+  if (!x || !y) return MOEQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y)) return MOEQ_ERR_ALIGN;
+  if (!shapes_fit(L, 1)) return MOEQ_ERR_SHAPE;
+  const DecodeWs wl = decode_ws_layout(L->H, L->I, L->E, L->k, L->has_shared, 1);
+  if (wl.total > kStaticScratchBytes) return MOEQ_ERR_WORKSPACE;
+  void* ws = static_scratch(device_info().device);
+  if (!ws) return MOEQ_ERR_CUDA;
+  // the counters must start at zero: clear them on every call, so that a call
+  // that ended in a device error does not leave stale counts for the next one
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = cuda_status(cudaMemsetAsync(static_cast<uint8_t*>(ws) + wl.ctr, 0, 4 * wl.n_ctr, s));
+  if (rc) return rc;
+  DecodeArgs a{};
+  fill_args(a, L, 1, x, y, ws, wl, dev_status, nullptr);
+  return launch<1>(a, false, stream);
 }

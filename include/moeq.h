@@ -181,6 +181,27 @@ int moe_route_topk(const uint16_t* x, int T, const uint16_t* router, int E, int 
 int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, void* ws, size_t ws_bytes,
                    int32_t* dev_status, const moeq_debug* dbg, moeq_stream stream);
 
+/* Batch-1 decode like moe_ffn_decode, for callers that cannot allocate device
+ * memory (for example a C program or a foreign runtime that holds device
+ * pointers to the weights and activations but has no device allocator): the
+ * scratch is a static array of the library, 160 KiB per device, instead of a
+ * caller workspace. This entry point has no counterpart on the source pages.
+ *   - Shapes whose decode workspace (moe_ffn_workspace(L, 1, 0)) exceeds
+ *     160 KiB are rejected with MOEQ_ERR_WORKSPACE before anything is
+ *     enqueued (the decode layer H=4096, I=2048, E=256, k=6 + shared expert
+ *     needs 131.5 KiB).
+ *   - The scratch's counters must start at zero: each call clears them with
+ *     an enqueued memset before its kernel, so a call that ended in a device
+ *     error does not affect the next one.
+ *   - Every call on a device uses the same scratch: calls that may overlap in
+ *     time (different streams, or different host threads without ordering)
+ *     race on it and give wrong results. Order them, e.g. on one stream.
+ *   - The first call on a device looks up the scratch's address (host side,
+ *     no allocation); make that first call before any stream capture.
+ * Results are those of moe_ffn_decode; no debug output. */
+int moe_ffn_decode_static(const moeq_layer* L, const uint16_t* x, float* y, int32_t* dev_status,
+                          moeq_stream stream);
+
 /* q=4 verification ("DeepSeek V4 Flash: 284B model ...", section "Decode: up
  * to 32 tok/s": the verifier decodes each packed weight once and applies it
  * to all four columns): four columns x [4 x H] bf16, each routed

@@ -119,5 +119,15 @@ def test_entry_points_reject_bad_arguments_before_launch():
     need4 = lib.moe_ffn_workspace(C.byref(L), 4, 1)
     need1 = lib.moe_ffn_workspace(C.byref(L), 1, 0)
     assert need4 > need1 > 0
+    # library-owned scratch: a decode shape whose workspace exceeds 160 KiB is
+    # rejected before anything is enqueued
+    big = _layer(H=4096, I=4096, E=16, k=8)
+    big.gate = _mat(2, 4096, 4096, 16)
+    big.up = _mat(2, 4096, 4096, 16)
+    big.down = _mat(3, 4096, 4096, 16)
+    assert lib.moe_ffn_workspace(C.byref(big), 1, 0) > 160 * 1024
+    assert lib.moe_ffn_decode_static(C.byref(big), FAKE, FAKE, None, None) == \
+        M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert lib.moe_ffn_decode_static(C.byref(L), None, FAKE, None, None) == M.CODE["MOEQ_ERR_ARG"]
     assert lib.h32_rotate(None, None, 4, None, None) == M.CODE["MOEQ_ERR_ARG"]
     assert lib.moe_rmsnorm_bf16(FAKE, 1, 100, FAKE, None) == M.CODE["MOEQ_ERR_SHAPE"]
