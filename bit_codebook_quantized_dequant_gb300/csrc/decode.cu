@@ -51,6 +51,7 @@
 // Geometric" (fused matvec, sync-free MoE decode).
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "moeq.h"
@@ -134,7 +135,7 @@ struct alignas(128) DecodeSmem {
   uint64_t empty[kStages];
   int unit[kStages];
   uint64_t rkey[kGroupWarps * kMaxK];  // routing item: per-warp candidate keys
-  uint32_t stage_cb[kStages][8];       // codebook records of the fill in each stage
+  alignas(16) uint32_t stage_cb[kStages][8];  // codebook records of the fill in each stage (bulk-copy target)
   float rwarp[kMaxCols * kGroupWarps];  // routing item: softmax partial sums per 64 logits
   float hs_first[kGroups][COLS][kGuRows];   // h of a first-half gate/up fill, by group
   float hs_second[kGroups][COLS][kGuRows];  // h of a second-half gate/up fill, by group
@@ -150,6 +151,12 @@ struct alignas(128) DecodeSmem {
   int issued;             // stage fills issued by the producer
   int consumed[kGroups];  // last stage fill waited for by each compute group
 };
+
+// Bulk asynchronous copies land in stage[] and stage_cb[]: both 16-byte aligned.
+static_assert(offsetof(DecodeSmem<1>, stage_cb) % 16 == 0 && offsetof(DecodeSmem<4>, stage_cb) % 16 == 0,
+              "bulk-copy targets must be 16-byte aligned");
+static_assert(offsetof(DecodeSmem<1>, stage) % 128 == 0 && offsetof(DecodeSmem<4>, stage) % 128 == 0,
+              "bulk-copy targets must be 16-byte aligned");
 
 // Item -> its first fill and number of fills (nu: routed units, needed only
 // past the routing item).

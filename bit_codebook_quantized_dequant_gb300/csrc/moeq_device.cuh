@@ -66,11 +66,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase; false when the limit ran out.
+// Bounded wait on an mbarrier phase; false when the limit ran out. Each try
+// may suspend the thread in hardware (up to 0.5 us) until the phase completes.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 16) __nanosleep(64);
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 500;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
   }
   return false;
 }
@@ -175,17 +183,18 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
 // FP2: cb = entries 0..3 in one word; w0, w1 the block's words.
 __device__ __forceinline__ int dot_fp2(uint32_t w0, uint32_t w1, uint32_t cb, const int* q) {
   uint32_t a = w0 & 0x33333333u, b = (w0 >> 2) & 0x33333333u;
+  // two independent accumulation chains (exact integer sums; shorter dependency)
   int s = __dp4a(static_cast<int>(prmt(cb, cb, a)), q[0], 0);
-  s = __dp4a(static_cast<int>(prmt(cb, cb, a >> 16)), q[1], s);
+  int s2 = __dp4a(static_cast<int>(prmt(cb, cb, a >> 16)), q[1], 0);
   s = __dp4a(static_cast<int>(prmt(cb, cb, b)), q[2], s);
-  s = __dp4a(static_cast<int>(prmt(cb, cb, b >> 16)), q[3], s);
+  s2 = __dp4a(static_cast<int>(prmt(cb, cb, b >> 16)), q[3], s2);
   a = w1 & 0x33333333u;
   b = (w1 >> 2) & 0x33333333u;
   s = __dp4a(static_cast<int>(prmt(cb, cb, a)), q[4], s);
-  s = __dp4a(static_cast<int>(prmt(cb, cb, a >> 16)), q[5], s);
+  s2 = __dp4a(static_cast<int>(prmt(cb, cb, a >> 16)), q[5], s2);
   s = __dp4a(static_cast<int>(prmt(cb, cb, b)), q[6], s);
-  s = __dp4a(static_cast<int>(prmt(cb, cb, b >> 16)), q[7], s);
-  return s;
+  s2 = __dp4a(static_cast<int>(prmt(cb, cb, b >> 16)), q[7], s2);
+  return s + s2;
 }
 
 // FP3 selectors for the four (w, h) groups of 8 elements: low two bits from
@@ -208,14 +217,14 @@ __device__ __forceinline__ int dot_fp3(uint32_t w0, uint32_t w1, uint32_t w2, ui
                                        uint32_t cb1, const int* q) {
   Fp3Sel t = fp3_selectors(w0, w1, w2);
   int s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s00)), q[0], 0);
-  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s00 >> 16)), q[1], s);
+  int s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s00 >> 16)), q[1], 0);
   s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s01)), q[2], s);
-  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s01 >> 16)), q[3], s);
+  s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s01 >> 16)), q[3], s2);
   s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s10)), q[4], s);
-  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s10 >> 16)), q[5], s);
+  s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s10 >> 16)), q[5], s2);
   s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s11)), q[6], s);
-  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s11 >> 16)), q[7], s);
-  return s;
+  s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s11 >> 16)), q[7], s2);
+  return s + s2;
 }
 
 // FP4 expansion of one word (8 codes in nibbles) into two words of int8 values.
@@ -239,17 +248,17 @@ __device__ __forceinline__ int dot_fp4(uint4 wd, const uint32_t* cb, const int* 
   uint32_t v0, v1;
   fp4_expand(wd.x, cb[0], cb[1], cb[2], cb[3], v0, v1);
   int s = __dp4a(static_cast<int>(v0), q[0], 0);
-  s = __dp4a(static_cast<int>(v1), q[1], s);
+  int s2 = __dp4a(static_cast<int>(v1), q[1], 0);
   fp4_expand(wd.y, cb[0], cb[1], cb[2], cb[3], v0, v1);
   s = __dp4a(static_cast<int>(v0), q[2], s);
-  s = __dp4a(static_cast<int>(v1), q[3], s);
+  s2 = __dp4a(static_cast<int>(v1), q[3], s2);
   fp4_expand(wd.z, cb[0], cb[1], cb[2], cb[3], v0, v1);
   s = __dp4a(static_cast<int>(v0), q[4], s);
-  s = __dp4a(static_cast<int>(v1), q[5], s);
+  s2 = __dp4a(static_cast<int>(v1), q[5], s2);
   fp4_expand(wd.w, cb[0], cb[1], cb[2], cb[3], v0, v1);
   s = __dp4a(static_cast<int>(v0), q[6], s);
-  s = __dp4a(static_cast<int>(v1), q[7], s);
-  return s;
+  s2 = __dp4a(static_cast<int>(v1), q[7], s2);
+  return s + s2;
 }
 
 // Generic: block (codes at p, shared or global memory) dotted with q, for the
@@ -298,9 +307,13 @@ __device__ __forceinline__ void block_expand(const uint8_t* p, const uint32_t* c
 // Dot product of an expanded block with 32 int8 activations (exact int32).
 __device__ __forceinline__ int dot8(const uint32_t (&v)[8], const int* q) {
   int s = __dp4a(static_cast<int>(v[0]), q[0], 0);
+  int s2 = __dp4a(static_cast<int>(v[1]), q[1], 0);
 #pragma unroll
-  for (int i = 1; i < 8; ++i) s = __dp4a(static_cast<int>(v[i]), q[i], s);
-  return s;
+  for (int i = 2; i < 8; i += 2) {
+    s = __dp4a(static_cast<int>(v[i]), q[i], s);
+    s2 = __dp4a(static_cast<int>(v[i + 1]), q[i + 1], s2);
+  }
+  return s + s2;
 }
 
 template <int FMT>
