@@ -145,6 +145,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
+def rank_token_start(rank: int, ntok: int) -> int:
+    """First token of a rank's own stream: ranks decode disjoint token ranges
+    (independent problems, no data-path collective)."""
+    return rank * ntok
+
+
+def max_over_ranks(times_ms, dist=None, device=None):
+    """Each rank's timed durations -> the maximum over ranks (the job's time)."""
+    import torch
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(world: int, units_per_rank: int, ms: float) -> float:
+    """Whole-job units per second: all ranks' units over the max-over-ranks time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -351,7 +371,7 @@ def run(args):
     layers = [build_layer(seed, r, cfg) for r in range(R)]
     wss = [Workspace(dl, 0) for dl in layers]
     ntok = 1024
-    xs_host = S.tokens(seed, cfg, ntok, start=rank * ntok)
+    xs_host = S.tokens(seed, cfg, ntok, start=rank_token_start(rank, ntok))
     xs = to_dev_u16(xs_host)                      # [ntok, H] resident in HBM
     H = cfg["H"]
     y = torch.zeros(H, dtype=torch.float32, device="cuda")
@@ -407,9 +427,7 @@ def run(args):
     ms_e2e = e0.elapsed_time(e1)
 
     if dist:
-        t = torch.tensor([ms, ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+        ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, device="cuda")
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -419,8 +437,8 @@ def run(args):
     per_tok = algorithmic_bytes_decode(cfg)
     ms_step = ms / args.steps
     achieved = per_tok / (ms_step * 1e-3) / 1e9
-    value = world * args.steps / (ms * 1e-3)
-    e2e = world * args.steps / (ms_e2e * 1e-3)
+    value = job_throughput(world, args.steps, ms)
+    e2e = job_throughput(world, args.steps, ms_e2e)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         tps, sample, _ = cpu_baseline(CFG_ID, 20)
