@@ -1,35 +1,40 @@
 // Grouped GEMMs of the prefill on the 5th-generation tensor cores (tcgen05).
 //
-// One tile = 128 weight rows x 64 grouped rows (tokens of one expert), the
-// whole contraction K in 32-element blocks. Per block the exact integer dot
-// products S[r, t] = sum_j cb[code] q are formed by tcgen05.mma kind::f16 on
-// bf16 operands (|cb|, |q| <= 127: every product and every 32-term sum is
-// exact in the fp32 accumulator), and the epilogue warps promote them with
-// the block scales in fp32, acc = fma(ws[r,b] * xd[t,b], S, acc), in block
-// order -- the same operations as the CUDA-core formulation, so the results
-// are those of the decode's arithmetic up to the order of the final sums.
+// One tile = 128 weight rows x 128 grouped rows (tokens of one expert), the
+// whole contraction K. The block scales are folded into the operands and the
+// operands split into bf16 parts so that every tensor-core product is exact:
+//   weights  a = cb[code] * ws[r, b]   (<= 19 significant bits, exact in fp32)
+//   activ.   x = q * d[t, b]            (<= 18 significant bits, exact in fp32)
+//   a = a_hi + a_lo, x = x_hi + x_lo with a_hi = bf16(a), a_lo = bf16(a - a_hi)
+//   (the part left out is below 2^-16 of the value; for power-of-two (E8M0)
+//   weight scales a is a bf16 value itself and a_lo = 0)
+// and a . x = sum of the part products, each exact in the fp32 accumulator.
+// tcgen05.mma kind::f16 accumulates the parts and all 32-element blocks of K
+// into one TMEM accumulator per tile, read out once per tile -- no per-block
+// hand-off between the tensor cores and the CUDA cores. The only difference to
+// the per-block formulation is the order of the fp32 sums (and the parts' last
+// bits), well inside the FFN output tolerance.
+//
+// Three GEMMs per expert kind: gate (epilogue: g to memory), up (epilogue:
+// h = silu(g) u, H32 and Q8 of the 32-block of h, which is the 32 rows of one
+// warp, and h's parts for the down GEMM), down (epilogue: the fp32 rows).
 //
 // Warp roles (16 warps):
-//   0-3   expansion: thread = weight row; packed codes arrive by cp.async into
-//         a per-row shared buffer, are expanded to bf16 with byte-permute
-//         lookups in the codebook (low and high bytes of the bf16 values) and
-//         written in the 128-byte-swizzled K-major layout of the MMA operand;
-//         the row's block scales go to the scale ring
-//   4     activation producer: one TMA (cp.async.bulk.tensor, SWIZZLE_128B)
-//         per 2 blocks of the tile's 64 grouped bf16 rows; their block scales
-//         go to the scale ring
-//   5     MMA issuer (one thread) and TMEM owner (512 columns)
-//   8-15  epilogue: two warpgroups, each the 128 rows x 32 columns of the
-//         accumulators (gate and up for the gate/up GEMM); tcgen05.ld per
-//         block, promotion, then SwiGLU + H32 + Q8 of h (a 32-block of h is
-//         the 32 rows of one warp) or the fp32 output rows.
-// Rings (mbarriers, every wait bounded): operand slots (2 blocks each), TMEM
-// accumulator buffers (1 block each), scale slots (2 blocks each).
+//   0-3   expansion: thread = weight row; packed codes and block scales arrive
+//         by cp.async into a per-row buffer; per block the codebook scaled by
+//         the block scale is split into bf16 parts and looked up with byte
+//         permutes, written in the 128-byte-swizzled K-major operand layout
+//   4     activation producer: TMA (SWIZZLE_128B) of the tile's 128 grouped
+//         rows, parts hi and lo, 64 K-elements per stage
+//   5     MMA issuer (one thread) and TMEM owner
+//   8-15  epilogue: two warpgroups, 64 columns each, once per tile
+// Rings (mbarriers, every wait bounded): 2 operand stages, 2 TMEM tile
+// accumulators (the epilogue of one tile overlaps the next tile's main loop).
 //
 // Sources: "DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
 // 395", section "ROCmFPX: fitting 284B weights into 128 GB" (small codebooks
-// expanded on the fly, integer dot products); "deepseek-v4-flash-0731-evox3-
-// rocm", section "The optimization ladder" (fused multi-token prefill with H32).
+// expanded on the fly); "deepseek-v4-flash-0731-evox3-rocm", section "The
+// optimization ladder" (fused multi-token prefill with H32).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -41,53 +46,47 @@
 namespace moeq {
 namespace {
 
-constexpr int kTM = 128;       // weight rows per tile
-constexpr int kTN = 64;        // grouped rows per tile
-constexpr int kKC = 8;         // 32-blocks per raw code chunk
-constexpr int kSlots = 3;      // operand slots (2 blocks each)
-constexpr int kBufs = 4;       // TMEM accumulator buffers (1 block each)
-constexpr int kScs = 6;        // scale slots (2 blocks each)
-constexpr int kXd = 4;         // pairs the activation scales are fetched ahead
-constexpr int kXr = 8;         // their staging ring (> kXd)
+constexpr int kTM = 128;        // weight rows per tile
+constexpr int kTN = 128;        // grouped rows per tile
+constexpr int kKC = 8;          // 32-blocks per raw code chunk
+constexpr int kStages = 2;      // operand stages (64 K-elements each)
+constexpr int kAccBufs = 2;     // TMEM tile accumulators
 constexpr int kTcThreads = 512;
 constexpr int kBWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kEpiWarp0 = 8;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = kAccBufs * kTN;
 
 template <int FMT>
 struct TcSmem {
+  static constexpr int NA = FMT == 4 ? 1 : 2;  // weight parts
   static constexpr int BC = block_bytes<FMT>();
   // raw row: the chunk's codes, then its block scales (<= 16 B); the pitch
   // also keeps the rows of a warp on different banks
   static constexpr int RP = kKC * BC + 16;
-  uint8_t a[kSlots][2][kTM * 128];          // A operand: 128 rows x 64 bf16, SW128 K-major
-  uint8_t b[kSlots][kTN * 128];             // B operand: 64 rows x 64 bf16, SW128 K-major
-  uint8_t raw[2][2][kTM][RP];               // packed code chunks [stage][matrix][row]
-  float ws[kScs][2][2][kTM];                // weight block scales [slot][block][matrix][row]
-  float xd[kScs][2][kTN];                   // activation block scales [slot][block][row]
-  uint32_t xraw[kXr][kTN];                  // fp16 pairs of activation scales, kXd pairs ahead
-  uint64_t ab_full[kSlots], ab_empty[kSlots];
-  uint64_t acc_full[kBufs], acc_empty[kBufs];
-  uint64_t sc_full[kScs], sc_empty[kScs];
-  uint64_t drain;                           // completion of every MMA this CTA issued
+  uint8_t a[kStages][NA][kTM * 128];  // weight parts: 128 rows x 64 bf16, SW128 K-major
+  uint8_t b[kStages][2][kTN * 128];   // activation parts: 128 rows x 64 bf16, SW128 K-major
+  uint8_t raw[2][kTM][RP];            // packed code chunks [stage][row]
+  uint64_t full[kStages], empty[kStages];
+  uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
+  uint64_t drain;                     // completion of every MMA this CTA issued
   uint32_t tmem_base;
   volatile int abort;
 };
 
+enum EpiKind { EPI_G = 0, EPI_SWIGLU = 1, EPI_O = 2 };
+
 struct TcArgs {
-  int gu;
-  DMat wa, wb;
+  DMat w;
   int shared, g0, g1;
   const int* toff;
   const int* offsets;
   int K, R, rows;
-  const uint16_t* act_scale;  // fp16 [rows x K/32]
-  int8_t* hq;
-  uint16_t* hd;
-  uint16_t* hbf;
+  float* g;          // EPI_G: written, EPI_SWIGLU: read; [rows x R]
+  uint16_t* hhi;     // EPI_SWIGLU: h's parts for the down GEMM [rows x R]
+  uint16_t* hlo;
   const uint32_t* signs_h;
-  float* o;
+  float* o;          // EPI_O [rows x R]
   const int* pid;
   int T, k, ns;
   moeq_debug dbg;
@@ -128,26 +127,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Packed fp32 pairs (each lane an IEEE fp32 operation, round to nearest).
-__device__ __forceinline__ uint64_t pack2(float x, float y) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-  return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float& x, float& y) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -160,10 +139,9 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
 }
-// 4- or 8-byte asynchronous copies (cache-all variant); src_bytes 0 fills zeros.
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" :: "r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-               : "memory");
+// 4- or 8-byte asynchronous copies (cache-all variant).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
@@ -204,22 +182,47 @@ __device__ __forceinline__ bool warp_wait(TcSmem<FMT>& sm, uint64_t* bar, uint32
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// ---------------------------------------------------------------- codebook expansion to bf16
-__device__ __forceinline__ uint32_t bf16_bits_of_int(int v) {
-  return __float_as_uint(static_cast<float>(v)) >> 16;  // exact for |v| < 256
+// ---------------------------------------------------------------- operand parts
+// Two fp32 values -> bf16 pair (round to nearest even), lower half = x.
+__device__ __forceinline__ uint32_t bf16x2_rn(float x, float y) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(y), "f"(x));
+  return r;
+}
+__device__ __forceinline__ float bf16_lo_f(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
+
+// hi/lo bf16 parts of four fp32 values (v = hi + lo up to the bits below 2^-16
+// of v): hi pairs and lo pairs, elements (0, 1) and (2, 3).
+__device__ __forceinline__ void split4(const float* v, uint32_t* hi, uint32_t* lo) {
+  hi[0] = bf16x2_rn(v[0], v[1]);
+  hi[1] = bf16x2_rn(v[2], v[3]);
+  lo[0] = bf16x2_rn(__fsub_rn(v[0], bf16_lo_f(hi[0])), __fsub_rn(v[1], bf16_hi_f(hi[0])));
+  lo[1] = bf16x2_rn(__fsub_rn(v[2], bf16_lo_f(hi[1])), __fsub_rn(v[3], bf16_hi_f(hi[1])));
 }
 
-// Low and high bytes of the bf16 values of a codebook of n entries, 4 per word.
-__device__ __forceinline__ void cb_tables(const int8_t* cb, int n, uint32_t* lo, uint32_t* hi) {
-  for (int w = 0; w < n / 4; ++w) {
-    uint32_t l = 0, h = 0;
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t b = bf16_bits_of_int(cb[4 * w + j]);
-      l |= (b & 0xffu) << (8 * j);
-      h |= (b >> 8) << (8 * j);
-    }
-    lo[w] = l;
-    hi[w] = h;
+// Byte planes (low bytes, high bytes) of four bf16 values given as two pairs.
+__device__ __forceinline__ void planes(uint32_t p01, uint32_t p23, uint32_t& lo, uint32_t& hi) {
+  lo = prmt(p01, p23, 0x6420u);
+  hi = prmt(p01, p23, 0x7531u);
+}
+
+// The codebook scaled by one block scale, split into bf16 parts, as byte
+// planes for the permute lookups: tl/th of the hi part, ul/uh of the lo part
+// (1 << FMT entries, 4 per word). cbf: the codebook as fp32.
+template <int FMT>
+__device__ __forceinline__ void scaled_tables(const float* cbf, float ws, uint32_t* tl, uint32_t* th,
+                                              uint32_t* ul, uint32_t* uh) {
+  constexpr int NV = 1 << FMT;
+#pragma unroll
+  for (int w = 0; w < NV / 4; ++w) {
+    float t[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) t[j] = __fmul_rn(cbf[4 * w + j], ws);  // exact: <= 19 significant bits
+    uint32_t hp[2], lp[2];
+    split4(t, hp, lp);
+    planes(hp[0], hp[1], tl[w], th[w]);
+    if constexpr (FMT != 4) planes(lp[0], lp[1], ul[w], uh[w]);
   }
 }
 
@@ -229,7 +232,8 @@ __device__ __forceinline__ void interleave4(uint32_t lo, uint32_t hi, uint32_t* 
   out[1] = prmt(lo, hi, 0x7362u);
 }
 
-// One block (32 codes at p) -> 16 words of bf16 pairs (elements 2i, 2i+1 in word i).
+// One block (32 codes at p) -> 16 words of bf16 pairs (elements 2i, 2i+1 in
+// word i), values from the byte planes tl (low bytes) and th (high bytes).
 template <int FMT>
 __device__ __forceinline__ void expand_bf16(const uint8_t* p, const uint32_t* tl, const uint32_t* th,
                                             uint32_t* out) {
@@ -262,6 +266,17 @@ __device__ __forceinline__ void expand_bf16(const uint8_t* p, const uint32_t* tl
       interleave4(l0, h0, out + 4 * q);
       interleave4(l1, h1, out + 4 * q + 2);
     }
+  }
+}
+
+// Writes a block's 16 words (32 bf16, K-elements 32 hb .. 32 hb + 31 of the
+// stage) into row r of a 128-byte-swizzled K-major operand tile.
+__device__ __forceinline__ void put_row(uint8_t* tile, int r, int hb, const uint32_t* v) {
+  uint8_t* rowp = tile + r * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int ch = (4 * hb + i) ^ (r & 7);
+    *reinterpret_cast<uint4*>(rowp + 16 * ch) = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   }
 }
 
@@ -299,46 +314,30 @@ __device__ __forceinline__ void pid_split(const TcArgs& a, int pid, int& t, int&
   }
 }
 
-// Timeline event of CTA 0 (debug only): role 0 expansion, 1 producer, 2 MMA,
-// 3 epilogue; (globaltimer ns, event << 32 | counter).
-__device__ __forceinline__ void tc_trace(const TcArgs& a, int role, int& n, uint32_t ev, int ctr) {
-  if (a.dbg.trace && blockIdx.x == 0 && n < a.dbg.trace_cap) {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    uint64_t* p = a.dbg.trace + 2 * (static_cast<size_t>(role) * a.dbg.trace_cap + n);
-    p[0] = t;
-    p[1] = (static_cast<uint64_t>(ev) << 32) | static_cast<uint32_t>(ctr);
-  }
-  ++n;
-}
-
 // ---------------------------------------------------------------- kernel
-template <int FMT, bool GU>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_hi,
+                                                                const __grid_constant__ CUtensorMap tm_lo,
                                                                 const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   TcSmem<FMT>& sm = *reinterpret_cast<TcSmem<FMT>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int BC = block_bytes<FMT>();
-  constexpr int NM = GU ? 2 : 1;
+  constexpr int NA = TcSmem<FMT>::NA;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = a.K / 32;
-  const int npairs = nb / 2;
+  const int nstages = a.K / 64;
   const int t_begin = __ldg(&a.toff[a.g0]);
   const int ntiles = __ldg(&a.toff[a.g1]) - t_begin;
 
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&sm.ab_full[i], 5);   // 4 expansion warps + the activation producer (+ its bytes)
-      mbar_init(&sm.ab_empty[i], 1);  // MMA commit
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.full[i], 5);   // 4 expansion warps + the activation producer (+ its bytes)
+      mbar_init(&sm.empty[i], 1);  // MMA commit
     }
-    for (int i = 0; i < kBufs; ++i) {
-      mbar_init(&sm.acc_full[i], 1);  // MMA commit
-      mbar_init(&sm.acc_empty[i], 8); // epilogue warps
-    }
-    for (int i = 0; i < kScs; ++i) {
-      mbar_init(&sm.sc_full[i], 5);
-      mbar_init(&sm.sc_empty[i], 8);
+    for (int i = 0; i < kAccBufs; ++i) {
+      mbar_init(&sm.acc_full[i], 1);   // MMA commit
+      mbar_init(&sm.acc_empty[i], 8);  // epilogue warps
     }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -357,38 +356,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   if (warp < 4) {
     // ------------------------------------------------------------ expansion (thread = row)
     const int r = tid;
-    int ks = 0, ntr = 0;
+    int ks = 0;
+    constexpr int NV = 1 << FMT;
     for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
       const TileInfo t = tile_info(a, t_begin + ti);
-      uint32_t tl[2][4], th[2][4];
+      float cbf[NV];
+      const int8_t* cb = a.w.cb + static_cast<size_t>(t.e) * a.w.cb_stride;
 #pragma unroll
-      for (int m = 0; m < NM; ++m) {
-        const DMat& M = m == 0 ? a.wa : a.wb;
-        cb_tables(M.cb + static_cast<size_t>(t.e) * M.cb_stride, 1 << FMT, tl[m], th[m]);
-      }
+      for (int v = 0; v < NV; ++v) cbf[v] = static_cast<float>(cb[v]);
       const size_t row = static_cast<size_t>(t.m0 + r);
       // one chunk of the row: its codes and its block scales, by asynchronous copies
       auto issue_chunk = [&](int c) {
         constexpr int SB = FMT == 4 ? 1 : 2;
         const int kc = c * kKC, kb = min(kKC, nb - kc);
-        const int pieces = kb * BC / 16;
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          const DMat& M = m == 0 ? a.wa : a.wb;
-          const uint8_t* src = M.codes + static_cast<size_t>(t.e) * M.stride_codes + (row * nb + kc) * BC;
-          uint8_t* dst = sm.raw[c & 1][m][r];
-          for (int i = 0; i < pieces; ++i) cp_async16(dst + 16 * i, src + 16 * i);
-          const size_t soff = (row * nb + kc) * SB;
-          const uint8_t* ssrc = M.scales + static_cast<size_t>(t.e) * M.stride_scales + soff;
-          uint8_t* sdst = dst + kKC * BC;
-          const int sbytes = kb * SB;  // 4, 8 or 16; soff is aligned to the piece used
-          if (sbytes % 16 == 0 && soff % 16 == 0) {
-            for (int i = 0; i < sbytes; i += 16) cp_async16(sdst + i, ssrc + i);
-          } else if (sbytes % 8 == 0 && soff % 8 == 0) {
-            for (int i = 0; i < sbytes; i += 8) cp_async8(sdst + i, ssrc + i);
-          } else {
-            for (int i = 0; i < sbytes; i += 4) cp_async4(sdst + i, ssrc + i, 4);
-          }
+        const uint8_t* src = a.w.codes + static_cast<size_t>(t.e) * a.w.stride_codes + (row * nb + kc) * BC;
+        uint8_t* dst = sm.raw[c & 1][r];
+        for (int i = 0; i < kb * BC / 16; ++i) cp_async16(dst + 16 * i, src + 16 * i);
+        const size_t soff = (row * nb + kc) * SB;
+        const uint8_t* ssrc = a.w.scales + static_cast<size_t>(t.e) * a.w.stride_scales + soff;
+        uint8_t* sdst = dst + kKC * BC;
+        const int sbytes = kb * SB;  // 4, 8 or 16; soff is aligned to the piece used
+        if (sbytes % 16 == 0 && soff % 16 == 0) {
+          for (int i = 0; i < sbytes; i += 16) cp_async16(sdst + i, ssrc + i);
+        } else if (sbytes % 8 == 0 && soff % 8 == 0) {
+          for (int i = 0; i < sbytes; i += 8) cp_async8(sdst + i, ssrc + i);
+        } else {
+          for (int i = 0; i < sbytes; i += 4) cp_async4(sdst + i, ssrc + i);
         }
         cp_async_commit();
       };
@@ -401,48 +394,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         } else {
           cp_async_wait<0>();
         }
-        if (tid == 0) tc_trace(a, 0, ntr, 4, c);
         const int kc = c * kKC, kb = min(kKC, nb - kc);
+        const uint8_t* rawr = sm.raw[c & 1][r];
         for (int jp = 0; jp < kb / 2; ++jp, ++ks) {
-          const int slot = ks % kSlots, scs = ks % kScs;
-          if (tid == 0) tc_trace(a, 0, ntr, 1, ks);
-          if (ks >= kSlots && !warp_wait<FMT>(sm, &sm.ab_empty[slot], ((ks / kSlots) - 1) & 1, a.status, lane)) break;
-          if (tid == 0) tc_trace(a, 0, ntr, 2, ks);
-          float wsr[NM][2];
+          const int slot = ks % kStages;
+          if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status, lane)) break;
 #pragma unroll
-          for (int m = 0; m < NM; ++m)
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-              const uint8_t* sp = &sm.raw[c & 1][m][r][kKC * BC];
-              if constexpr (FMT == 4) wsr[m][hb] = e8m0_to_f32(sp[2 * jp + hb]);
-              else wsr[m][hb] = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(sp)[2 * jp + hb]);
-            }
-#pragma unroll
-          for (int m = 0; m < NM; ++m) {
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-              uint32_t v[16];
-              expand_bf16<FMT>(&sm.raw[c & 1][m][r][(2 * jp + hb) * BC], tl[m], th[m], v);
-              uint8_t* rowp = sm.a[slot][m] + r * 128;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int ch = (4 * hb + i) ^ (r & 7);
-                *reinterpret_cast<uint4*>(rowp + 16 * ch) = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-              }
+          for (int hb = 0; hb < 2; ++hb) {
+            const int jb = 2 * jp + hb;
+            float ws;
+            if constexpr (FMT == 4) ws = e8m0_to_f32(rawr[kKC * BC + jb]);
+            else ws = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(rawr + kKC * BC)[jb]);
+            uint32_t tl[4], th[4], ul[4], uh[4];
+            scaled_tables<FMT>(cbf, ws, tl, th, ul, uh);
+            uint32_t v[16];
+            expand_bf16<FMT>(rawr + jb * BC, tl, th, v);
+            put_row(sm.a[slot][0], r, hb, v);
+            if constexpr (NA == 2) {
+              expand_bf16<FMT>(rawr + jb * BC, ul, uh, v);
+              put_row(sm.a[slot][NA - 1], r, hb, v);
             }
           }
-          if (tid == 0) tc_trace(a, 0, ntr, 3, ks);
-          if (ks >= kScs && !warp_wait<FMT>(sm, &sm.sc_empty[scs], ((ks / kScs) - 1) & 1, a.status, lane)) break;
-#pragma unroll
-          for (int m = 0; m < NM; ++m)
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) sm.ws[scs][hb][m][r] = wsr[m][hb];
           fence_proxy_async();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&sm.ab_full[slot]);
-            mbar_arrive(&sm.sc_full[scs]);
-          }
+          if (lane == 0) mbar_arrive(&sm.full[slot]);
         }
         if (sm.abort) break;
       }
@@ -450,83 +425,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     cp_async_wait<0>();
   } else if (warp == kBWarp) {
     // ------------------------------------------------------------ activation producer
-    int ks = 0, ntr = 0;
+    int ks = 0;
     for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
       const TileInfo t = tile_info(a, t_begin + ti);
       const int y0 = t.off + t.tt * kTN;
-      // the 2 fp16 scales of a pair for rows lane and lane + 32, kXd pairs ahead
-      // (one copy group per pair; a lane only reads what it copied)
-      auto fetch_xd = [&](int p) {
-        if (p < npairs) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = lane + 32 * h, jr = t.tt * kTN + j;
-            const uint16_t* src = a.act_scale + static_cast<size_t>(t.off + (jr < t.n ? jr : 0)) * nb + 2 * p;
-            cp_async4(&sm.xraw[p % kXr][j], src, jr < t.n ? 4u : 0u);
-          }
-        }
-        cp_async_commit();
-      };
-      for (int p = 0; p < kXd; ++p) fetch_xd(p);
-      for (int p = 0; p < npairs; ++p, ++ks) {
-        const int slot = ks % kSlots, scs = ks % kScs;
-        if (ks >= kSlots && !warp_wait<FMT>(sm, &sm.ab_empty[slot], ((ks / kSlots) - 1) & 1, a.status, lane)) break;
-        if (lane == 0) tc_trace(a, 1, ntr, 2, ks);
+      for (int p = 0; p < nstages; ++p, ++ks) {
+        const int slot = ks % kStages;
+        if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status, lane)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.ab_full[slot], kTN * 128);
-          tma_load_2d(sm.b[slot], &tm_act, 64 * p, y0, &sm.ab_full[slot]);
-        }
-        if (ks >= kScs && !warp_wait<FMT>(sm, &sm.sc_empty[scs], ((ks / kScs) - 1) & 1, a.status, lane)) break;
-        fetch_xd(p + kXd);
-        cp_async_wait<kXd>();  // this pair's group has landed
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t v = sm.xraw[p % kXr][lane + 32 * h];
-          sm.xd[scs][0][lane + 32 * h] = f16_bits_to_f32(static_cast<uint16_t>(v & 0xffffu));
-          sm.xd[scs][1][lane + 32 * h] = f16_bits_to_f32(static_cast<uint16_t>(v >> 16));
+          mbar_arrive_expect_tx(&sm.full[slot], 2 * kTN * 128);
+          tma_load_2d(sm.b[slot][0], &tm_hi, 64 * p, y0, &sm.full[slot]);
+          tma_load_2d(sm.b[slot][1], &tm_lo, 64 * p, y0, &sm.full[slot]);
         }
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sm.sc_full[scs]);
-          tc_trace(a, 1, ntr, 5, ks);
-        }
       }
-      cp_async_wait<0>();
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
-      int ks = 0, kg = 0, ntr = 0;
+      int ks = 0, kt = 0;
       bool ok = true;
-      for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
-        for (int p = 0; p < npairs && ok; ++p, ++ks) {
-          const int slot = ks % kSlots;
-          if (!(ok = ring_wait<FMT>(sm, &sm.ab_full[slot], (ks / kSlots) & 1, a.status))) break;
-          tc_trace(a, 2, ntr, 2, ks);
+      for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x, ++kt) {
+        const int tb = kt % kAccBufs;
+        if (kt >= kAccBufs && !(ok = ring_wait<FMT>(sm, &sm.acc_empty[tb], ((kt / kAccBufs) - 1) & 1, a.status)))
+          break;
+        tc_fence_after();
+        const uint32_t dcol = tmem + static_cast<uint32_t>(tb * kTN);
+        for (int p = 0; p < nstages && ok; ++p, ++ks) {
+          const int slot = ks % kStages;
+          if (!(ok = ring_wait<FMT>(sm, &sm.full[slot], (ks / kStages) & 1, a.status))) break;
           tc_fence_after();
-          const uint32_t abase[2] = {smem_u32(sm.a[slot][0]), smem_u32(sm.a[slot][1])};
-          const uint32_t bbase = smem_u32(sm.b[slot]);
-#pragma unroll 1
-          for (int hb = 0; hb < 2; ++hb, ++kg) {
-            const int buf = kg % kBufs;
-            if (kg >= kBufs && !(ok = ring_wait<FMT>(sm, &sm.acc_empty[buf], ((kg / kBufs) - 1) & 1, a.status)))
-              break;
-            tc_trace(a, 2, ntr, 6, kg);
-            tc_fence_after();
-            const uint32_t dcol = tmem + static_cast<uint32_t>(buf * (GU ? 2 * kTN : kTN));
 #pragma unroll
-            for (int m = 0; m < NM; ++m) {
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t koff = static_cast<uint32_t>(kk * 32);
 #pragma unroll
-              for (int s = 0; s < 2; ++s) {
-                const uint32_t koff = static_cast<uint32_t>((2 * hb + s) * 32);
-                mma_bf16(dcol + static_cast<uint32_t>(m * kTN), sw128_desc(abase[m] + koff),
-                         sw128_desc(bbase + koff), s);
-              }
-            }
-            mma_commit(&sm.acc_full[buf]);
+            for (int pa = 0; pa < NA; ++pa)
+#pragma unroll
+              for (int pb = 0; pb < 2; ++pb)
+                mma_bf16(dcol, sw128_desc(smem_u32(sm.a[slot][pa]) + koff),
+                         sw128_desc(smem_u32(sm.b[slot][pb]) + koff),
+                         (p > 0 || kk > 0 || pa > 0 || pb > 0) ? 1u : 0u);
           }
-          if (ok) mma_commit(&sm.ab_empty[slot]);
+          mma_commit(&sm.empty[slot]);
         }
+        if (ok) mma_commit(&sm.acc_full[tb]);
       }
       // TMEM is released only after every MMA this thread issued has completed
       // (also when a wait above ran out and the loops were left early)
@@ -537,102 +479,60 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;           // TMEM lane quarter = rows 32q .. 32q + 31
-    const int half = (warp - kEpiWarp0) >> 2;
-    const int c0 = 32 * half;         // this warpgroup's 32 columns
+    // ------------------------------------------------------------ epilogue (once per tile)
+    const int q = warp & 3;                // TMEM lane quarter = rows 32q .. 32q + 31
+    const int c0 = 64 * ((warp - kEpiWarp0) >> 2);  // this warpgroup's 64 columns
     const int r = 32 * q + lane;
-    int ks = 0, kg = 0, ntr = 0;
-    bool ok = true;
-    for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x) {
+    int kt = 0;
+    for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x, ++kt) {
       const TileInfo t = tile_info(a, t_begin + ti);
-      uint64_t acc[NM][16];  // column pairs (2j, 2j + 1) of this warpgroup's 32 columns
+      const int tb = kt % kAccBufs;
+      if (!warp_wait<FMT>(sm, &sm.acc_full[tb], (kt / kAccBufs) & 1, a.status, lane)) break;
+      tc_fence_after();
+      float acc[64];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * kTN + c0);
 #pragma unroll
-      for (int m = 0; m < NM; ++m)
+      for (int i = 0; i < 4; ++i) tmem_ld16(taddr + 16 * i, acc + 16 * i);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[tb]);
+      const size_t rowcol = static_cast<size_t>(t.m0 + r);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[m][j] = 0ull;
-      for (int p = 0; p < npairs && ok; ++p, ++ks) {
-        const int scs = ks % kScs;
-        if (!(ok = warp_wait<FMT>(sm, &sm.sc_full[scs], (ks / kScs) & 1, a.status, lane))) break;
-#pragma unroll 1
-        for (int hb = 0; hb < 2; ++hb, ++kg) {
-          const int buf = kg % kBufs;
-          if (!(ok = warp_wait<FMT>(sm, &sm.acc_full[buf], (kg / kBufs) & 1, a.status, lane))) break;
-          if (tid == 32 * kEpiWarp0) tc_trace(a, 3, ntr, 6, kg);
-          tc_fence_after();
-          const float4* xdv = reinterpret_cast<const float4*>(&sm.xd[scs][hb][c0]);
-#pragma unroll
-          for (int m = 0; m < NM; ++m) {
-            const float wsv = sm.ws[scs][hb][m][r];
-            const uint64_t ws2 = pack2(wsv, wsv);
-            const uint32_t col = static_cast<uint32_t>(buf * (GU ? 2 * kTN : kTN) + m * kTN + c0);
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col;
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-              float S[16];
-              tmem_ld16(taddr + 16 * ch, S);
-              tmem_wait_ld();
-              // acc = fma(ws * xd, S, acc) per column, two columns per instruction
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float4 x4 = xdv[4 * ch + i];
-                const uint64_t sc0 = mul2(ws2, pack2(x4.x, x4.y));
-                const uint64_t sc1 = mul2(ws2, pack2(x4.z, x4.w));
-                acc[m][8 * ch + 2 * i] = fma2(sc0, pack2(S[4 * i], S[4 * i + 1]), acc[m][8 * ch + 2 * i]);
-                acc[m][8 * ch + 2 * i + 1] = fma2(sc1, pack2(S[4 * i + 2], S[4 * i + 3]), acc[m][8 * ch + 2 * i + 1]);
-              }
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
-          if (tid == 32 * kEpiWarp0) tc_trace(a, 3, ntr, 7, kg);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.sc_empty[scs]);
-      }
-      if (!ok) break;
-      if (tid == 32 * kEpiWarp0) tc_trace(a, 3, ntr, 8, ti);
-      // tile epilogue: 32 columns of this warpgroup; row m0 + r (unrolled:
-      // the accumulators stay in registers)
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 64; ++j) {
         const int jr = t.tt * kTN + c0 + j;
         if (jr >= t.n) continue;  // warp-uniform
         const size_t grow = static_cast<size_t>(t.off + jr);
-        float av[NM];
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          float lo, hi;
-          unpack2(acc[m][j / 2], lo, hi);
-          av[m] = (j & 1) ? hi : lo;
-        }
-        if constexpr (GU) {
-          const float g = av[0], u = av[NM - 1];
-          const float h = g * u / (1.0f + expf(-g));
+        const size_t at = grow * a.R + rowcol;
+        if constexpr (EPI == EPI_G) {
+          a.g[at] = acc[j];
+        } else if constexpr (EPI == EPI_O) {
+          a.o[at] = acc[j];
+          if (a.dbg.o) {
+            int tk, s;
+            pid_split(a, a.pid[grow], tk, s);
+            a.dbg.o[(static_cast<size_t>(tk) * a.ns + s) * a.R + rowcol] = acc[j];
+          }
+        } else {
+          const float gv = __ldcg(&a.g[at]), u = acc[j];
+          const float h = gv * u / (1.0f + expf(-gv));
           const int blk = (t.m0 + 32 * q) / 32;
-          float v = h;
-          if (a.signs_h) v = h32_warp(v, __ldg(&a.signs_h[blk]), lane);
+          float vv = h;
+          if (a.signs_h) vv = h32_warp(vv, __ldg(&a.signs_h[blk]), lane);
           uint16_t db;
-          const int8_t qv = q8_warp(v, db);
-          const size_t at = grow * a.R + t.m0 + r;
-          a.hq[at] = qv;
-          a.hbf[at] = static_cast<uint16_t>(bf16_bits_of_int(qv));
-          if (lane == 0) a.hd[grow * (a.R / 32) + blk] = db;
+          const int8_t qv = q8_warp(vv, db);
+          // h's parts for the down GEMM: q * d (exact in fp32) as bf16 hi + lo
+          const float pv = __fmul_rn(static_cast<float>(qv), f16_bits_to_f32(db));
+          const uint32_t hp = bf16x2_rn(pv, 0.0f);
+          a.hhi[at] = static_cast<uint16_t>(hp & 0xffffu);
+          a.hlo[at] = static_cast<uint16_t>(bf16x2_rn(__fsub_rn(pv, bf16_lo_f(hp)), 0.0f) & 0xffffu);
           if (a.dbg.h || a.dbg.hq || a.dbg.hd) {
             int tk, s;
             pid_split(a, a.pid[grow], tk, s);
             const size_t vec = static_cast<size_t>(tk) * a.ns + s;
-            if (a.dbg.h) a.dbg.h[vec * a.R + t.m0 + r] = h;
-            if (a.dbg.hq) a.dbg.hq[vec * a.R + t.m0 + r] = qv;
+            if (a.dbg.h) a.dbg.h[vec * a.R + rowcol] = h;
+            if (a.dbg.hq) a.dbg.hq[vec * a.R + rowcol] = qv;
             if (a.dbg.hd && lane == 0) a.dbg.hd[vec * (a.R / 32) + blk] = db;
-          }
-        } else {
-          a.o[grow * a.R + t.m0 + r] = av[0];
-          if (a.dbg.o) {
-            int tk, s;
-            pid_split(a, a.pid[grow], tk, s);
-            a.dbg.o[(static_cast<size_t>(tk) * a.ns + s) * a.R + t.m0 + r] = av[0];
           }
         }
       }
@@ -667,15 +567,35 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int FMT, bool GU>
-int launch_tc(const CUtensorMap& tm, const TcArgs& a, int grid, cudaStream_t s) {
+// bf16 [rows x K] activation parts, boxes of 64 K-elements x 128 rows, 128-byte swizzle.
+int act_map(EncodeTiledFn enc, CUtensorMap* tm, const uint16_t* base, int K, int rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64, kTN};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? MOEQ_OK
+             : MOEQ_ERR_CUDA;
+}
+
+template <int FMT, int EPI>
+int launch_tc(const CUtensorMap& th, const CUtensorMap& tl, const TcArgs& a, int grid, cudaStream_t s) {
   const size_t smem = sizeof(TcSmem<FMT>) + 1024;
   if (smem > device_info().max_smem_optin) return MOEQ_ERR_SHAPE;
-  if (cudaFuncSetAttribute(tc_gemm_kernel<FMT, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MOEQ_ERR_CUDA;
-  tc_gemm_kernel<FMT, GU><<<grid, kTcThreads, smem, s>>>(tm, a);
+  tc_gemm_kernel<FMT, EPI><<<grid, kTcThreads, smem, s>>>(th, tl, a);
   return cuda_status(cudaGetLastError());
+}
+
+template <int EPI>
+int launch_fmt(int fmt, const CUtensorMap& th, const CUtensorMap& tl, const TcArgs& a, int grid, cudaStream_t s) {
+  if (fmt == 2) return launch_tc<2, EPI>(th, tl, a, grid, s);
+  if (fmt == 3) return launch_tc<3, EPI>(th, tl, a, grid, s);
+  return launch_tc<4, EPI>(th, tl, a, grid, s);
 }
 
 }  // namespace
@@ -684,20 +604,12 @@ int tc_grouped_gemm(const TcGemm& g, cudaStream_t s) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return MOEQ_ERR_CUDA;
   if (g.K % 64 || g.R % kTM) return MOEQ_ERR_SHAPE;
-  // activations [rows x K] bf16, boxes of 64 K-elements x 64 rows, 128-byte swizzle
-  CUtensorMap tm;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(g.rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.K) * 2};
-  const cuuint32_t box[2] = {64, kTN};
-  const cuuint32_t es[2] = {1, 1};
-  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(g.act), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return MOEQ_ERR_CUDA;
+  CUtensorMap th, tl;
+  int rc = act_map(enc, &th, g.act_hi, g.K, g.rows);
+  if (!rc) rc = act_map(enc, &tl, g.act_lo, g.K, g.rows);
+  if (rc) return rc;
   TcArgs a{};
-  a.gu = g.gu;
-  a.wa = g.wa;
-  a.wb = g.wb;
+  a.w = g.w;
   a.shared = g.shared;
   a.g0 = g.g0;
   a.g1 = g.g1;
@@ -706,10 +618,9 @@ int tc_grouped_gemm(const TcGemm& g, cudaStream_t s) {
   a.K = g.K;
   a.R = g.R;
   a.rows = g.rows;
-  a.act_scale = g.act_scale;
-  a.hq = g.hq;
-  a.hd = g.hd;
-  a.hbf = g.hbf;
+  a.g = g.g;
+  a.hhi = g.hhi;
+  a.hlo = g.hlo;
   a.signs_h = g.signs_h;
   a.o = g.o;
   a.pid = g.pid;
@@ -719,15 +630,9 @@ int tc_grouped_gemm(const TcGemm& g, cudaStream_t s) {
   a.dbg = g.dbg;
   a.status = g.status;
   const int grid = device_info().sm_count;
-  const int fmt = g.wa.fmt;
-  if (g.gu) {
-    if (fmt == 2) return launch_tc<2, true>(tm, a, grid, s);
-    if (fmt == 3) return launch_tc<3, true>(tm, a, grid, s);
-    return launch_tc<4, true>(tm, a, grid, s);
-  }
-  if (fmt == 2) return launch_tc<2, false>(tm, a, grid, s);
-  if (fmt == 3) return launch_tc<3, false>(tm, a, grid, s);
-  return launch_tc<4, false>(tm, a, grid, s);
+  if (g.epi == EPI_G) return launch_fmt<EPI_G>(g.w.fmt, th, tl, a, grid, s);
+  if (g.epi == EPI_SWIGLU) return launch_fmt<EPI_SWIGLU>(g.w.fmt, th, tl, a, grid, s);
+  return launch_fmt<EPI_O>(g.w.fmt, th, tl, a, grid, s);
 }
 
 }  // namespace moeq

@@ -58,22 +58,23 @@ const DeviceInfo& device_info();
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOEQ_ERR_CUDA; }
 
 // One grouped GEMM of the prefill on the tensor cores (gemm_tc.cu): tiles of
-// 128 weight rows x 64 grouped rows over groups [g0, g1); gu = 1: gate and up
-// (wa, wb) with the SwiGLU + H32 + Q8 epilogue into hq / hd / hbf, gu = 0:
-// down (wa) into o. act: bf16 [rows x K] grouped activations (exact values of
-// the int8 codes), act_scale: their fp16 block scales [rows x K/32].
+// 128 weight rows x 128 grouped rows over groups [g0, g1) with matrix w
+// (expert = group, or expert 0 for the shared expert). act_hi / act_lo: the
+// bf16 parts [rows x K] of the grouped activations (code times block scale).
+// epi 0: write g [rows x R] fp32; 1: read g, SwiGLU + H32 + Q8 of h, write
+// h's parts hhi / hlo [rows x R]; 2: write o [rows x R] fp32.
 struct TcGemm {
-  int gu;
-  DMat wa, wb;
+  int epi;
+  DMat w;
   int shared, g0, g1;
   const int* toff;
   const int* offsets;
   int K, R, rows;
-  const uint16_t* act;
-  const uint16_t* act_scale;
-  int8_t* hq;
-  uint16_t* hd;
-  uint16_t* hbf;
+  const uint16_t* act_hi;
+  const uint16_t* act_lo;
+  float* g;
+  uint16_t* hhi;
+  uint16_t* hlo;
   const uint32_t* signs_h;
   float* o;
   const int* pid;

@@ -85,11 +85,12 @@ inline DecodeWs verify_ws_layout(int H, int I, int E, int k, int has_shared) {
 // routed expert in a stable order (ascending token, then slot), then the T
 // rows of the shared expert. pid[row] = token * k + slot for routed rows and
 // T * k + token for shared rows; pos[token * k + slot] = its row.
-// The tensor-core GEMMs read the activations as bf16 rows in grouped order:
-// xg [rows x H] (x's int8 codes, gathered), xdg [rows x H/32] (their fp16
-// scales), hbf [rows x I] (h's int8 codes).
+// The tensor-core GEMMs read the activations in grouped order as two bf16
+// parts of (code x block scale): xhi / xlo [rows x H] for x, hhi / hlo
+// [rows x I] for h; g [rows x I] fp32 holds the gate projection between the
+// gate and the up GEMM.
 struct PrefillWs {
-  size_t xq, xd, idx, p, counts, offsets, tiles_gu, tiles_dn, pid, pos, xg, xdg, hq, hd, hbf, o, total;
+  size_t xq, xd, idx, p, counts, offsets, tiles_gu, tiles_dn, pid, pos, xhi, xlo, g, hhi, hlo, o, total;
 };
 
 inline PrefillWs prefill_ws_layout(int H, int I, int E, int k, int has_shared, int T) {
@@ -108,11 +109,11 @@ inline PrefillWs prefill_ws_layout(int H, int I, int E, int k, int has_shared, i
   w.tiles_dn = off; off += align256(4 * (groups + 1));
   w.pid = off;      off += align256(4 * rows);
   w.pos = off;      off += align256(4 * Tk);
-  w.xg = off;       off += align256(2 * rows * H);
-  w.xdg = off;      off += align256(2 * rows * (H / 32));
-  w.hq = off;       off += align256(rows * I);
-  w.hd = off;       off += align256(2 * rows * (I / 32));
-  w.hbf = off;      off += align256(2 * rows * I);
+  w.xhi = off;      off += align256(2 * rows * H);
+  w.xlo = off;      off += align256(2 * rows * H);
+  w.g = off;        off += align256(4 * rows * I);
+  w.hhi = off;      off += align256(2 * rows * I);
+  w.hlo = off;      off += align256(2 * rows * I);
   w.o = off;        off += align256(4 * rows * H);
   w.total = off;
   return w;

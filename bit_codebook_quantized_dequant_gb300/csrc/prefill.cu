@@ -4,10 +4,10 @@
 //   Q8 of every 32-block of x (after H32)       prep_x_kernel
 //   stable counting sort of the (token, slot) pairs by expert
 //                                               count_kernel, place_kernel
-//   x's int8 codes as bf16 rows in grouped order gather_kernel
-//   grouped gate/up GEMM per expert on the tensor cores, epilogue SwiGLU,
-//   H32 and Q8 of h                             gemm_tc.cu
-//   grouped down GEMM per expert (tensor cores) gemm_tc.cu
+//   x's code x scale as bf16 parts, grouped     gather_kernel
+//   grouped gate GEMM, then up GEMM with the SwiGLU, H32 and Q8 of h in its
+//   epilogue, then down GEMM, per expert kind, on the tensor cores
+//                                               gemm_tc.cu
 //   gather-combine in slot order (+ residual)   combine_kernel
 // all enqueued on the caller's stream with no host synchronization; the tile
 // lists of the grouped GEMMs are built on the device from the expert counts.
@@ -26,7 +26,7 @@
 namespace moeq {
 namespace {
 
-constexpr int kNT = 64;   // grouped rows per GEMM tile (gemm_tc.cu)
+constexpr int kNT = 128;  // grouped rows per GEMM tile (gemm_tc.cu)
 constexpr int kMT = 128;  // weight rows per GEMM tile (gemm_tc.cu)
 
 struct PrefillArgs {
@@ -45,11 +45,11 @@ struct PrefillArgs {
   int* tiles_dn;
   int* pid;
   int* pos;
-  uint16_t* xg;
-  uint16_t* xdg;
-  int8_t* hq;
-  uint16_t* hd;
-  uint16_t* hbf;
+  uint16_t* xhi;
+  uint16_t* xlo;
+  float* g;
+  uint16_t* hhi;
+  uint16_t* hlo;
   float* o;
   const float* residual;
   float* y;
@@ -185,9 +185,10 @@ __global__ void place_kernel(const PrefillArgs a) {
   }
 }
 
-// Grouped activation rows for the tensor-core GEMM: row r of group order is
-// token t = the token of pid[r]; xg[r] = x's int8 codes of t as bf16 (exact),
-// xdg[r] = their fp16 block scales. One warp per grouped row.
+// Grouped activation parts for the tensor-core GEMM: row r of group order is
+// token t = the token of pid[r]; v = q * d (x's int8 code times its block
+// scale, exact in fp32) as xhi = bf16(v), xlo = bf16(v - xhi). One warp per
+// grouped row.
 __global__ void gather_kernel(const PrefillArgs a, int rows) {
   const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -197,29 +198,31 @@ __global__ void gather_kernel(const PrefillArgs a, int rows) {
   const int t = pid >= Tk ? pid - Tk : pid / a.k;
   const int nbH = a.H / 32;
   const int8_t* src = a.xq + static_cast<size_t>(t) * a.H;
-  uint16_t* dst = a.xg + static_cast<size_t>(r) * a.H;
-  for (int c = lane; c < a.H / 16; c += 32) {  // 16 codes per step
-    const int4 q = *reinterpret_cast<const int4*>(src + 16 * c);
-    const uint32_t w[4] = {static_cast<uint32_t>(q.x), static_cast<uint32_t>(q.y), static_cast<uint32_t>(q.z),
-                           static_cast<uint32_t>(q.w)};
-    uint32_t o[8];
+  const uint16_t* dsc = a.xd + static_cast<size_t>(t) * nbH;
+  uint16_t* dhi = a.xhi + static_cast<size_t>(r) * a.H;
+  uint16_t* dlo = a.xlo + static_cast<size_t>(r) * a.H;
+  for (int c = lane; c < a.H / 8; c += 32) {  // 8 elements per step
+    const uint2 q = *reinterpret_cast<const uint2*>(src + 8 * c);
+    const float d = f16_bits_to_f32(dsc[(8 * c) / 32]);
+    uint32_t hi[4], lo[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int v0 = static_cast<int8_t>(w[i] >> (16 * h));
-        const int v1 = static_cast<int8_t>(w[i] >> (16 * h + 8));
-        const uint32_t b0 = __float_as_uint(static_cast<float>(v0)) >> 16;
-        const uint32_t b1 = __float_as_uint(static_cast<float>(v1)) >> 16;
-        o[2 * i + h] = b0 | (b1 << 16);
-      }
+      const uint32_t w = i < 2 ? q.x : q.y;
+      const int sh = 16 * (i & 1);
+      const float v0 = __fmul_rn(static_cast<float>(static_cast<int8_t>(w >> sh)), d);
+      const float v1 = __fmul_rn(static_cast<float>(static_cast<int8_t>(w >> (sh + 8))), d);
+      uint32_t h;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(v1), "f"(v0));
+      const float r0 = __fsub_rn(v0, __uint_as_float(h << 16));
+      const float r1 = __fsub_rn(v1, __uint_as_float(h & 0xffff0000u));
+      uint32_t l;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l) : "f"(r1), "f"(r0));
+      hi[i] = h;
+      lo[i] = l;
     }
-    uint4* d = reinterpret_cast<uint4*>(dst + 16 * c);
-    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    *reinterpret_cast<uint4*>(dhi + 8 * c) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(dlo + 8 * c) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
-  for (int b = lane; b < nbH; b += 32)
-    a.xdg[static_cast<size_t>(r) * nbH + b] = a.xd[static_cast<size_t>(t) * nbH + b];
 }
 
 // y[t, :] = sum_s p[t, s] o[pos[t, s], :] (+ o_shared[t, :]) (+ residual[t, :]),
@@ -298,11 +301,11 @@ extern "C" int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, co
   a.tiles_dn = reinterpret_cast<int*>(w + wl.tiles_dn);
   a.pid = reinterpret_cast<int*>(w + wl.pid);
   a.pos = reinterpret_cast<int*>(w + wl.pos);
-  a.xg = reinterpret_cast<uint16_t*>(w + wl.xg);
-  a.xdg = reinterpret_cast<uint16_t*>(w + wl.xdg);
-  a.hq = reinterpret_cast<int8_t*>(w + wl.hq);
-  a.hd = reinterpret_cast<uint16_t*>(w + wl.hd);
-  a.hbf = reinterpret_cast<uint16_t*>(w + wl.hbf);
+  a.xhi = reinterpret_cast<uint16_t*>(w + wl.xhi);
+  a.xlo = reinterpret_cast<uint16_t*>(w + wl.xlo);
+  a.g = reinterpret_cast<float*>(w + wl.g);
+  a.hhi = reinterpret_cast<uint16_t*>(w + wl.hhi);
+  a.hlo = reinterpret_cast<uint16_t*>(w + wl.hlo);
   a.o = reinterpret_cast<float*>(w + wl.o);
   a.residual = residual;
   a.y = y;
@@ -332,42 +335,42 @@ extern "C" int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, co
   TcGemm g{};
   g.offsets = a.offsets;
   g.rows = rows;
-  g.hq = a.hq;
-  g.hd = a.hd;
-  g.hbf = a.hbf;
+  g.g = a.g;
+  g.hhi = a.hhi;
+  g.hlo = a.hlo;
   g.signs_h = a.signs_h;
   g.o = a.o;
   g.pid = a.pid;
   g.T = T;
   g.k = L->k;
   g.ns = a.ns;
-  g.dbg = a.dbg;
   g.status = dev_status;
-  for (int pass = 0; pass < 4; ++pass) {
-    const bool gu = pass < 2, shared = pass & 1;
+  // gate, then up (+SwiGLU, H32, Q8 of h), then down; routed and shared experts
+  for (int pass = 0; pass < 6; ++pass) {
+    const int stage = pass / 2;  // 0 gate, 1 up, 2 down
+    const bool shared = pass & 1;
     if (shared && !a.has_shared) continue;
-    g.gu = gu ? 1 : 0;
+    g.epi = stage;
     g.shared = shared ? 1 : 0;
     g.g0 = shared ? L->E : 0;
     g.g1 = shared ? L->E + 1 : L->E;
-    if (gu) {
-      g.wa = shared ? a.sgate : a.gate;
-      g.wb = shared ? a.sup : a.up;
+    g.dbg = a.dbg;
+    g.dbg.trace = nullptr;
+    if (stage < 2) {
+      g.w = stage == 0 ? (shared ? a.sgate : a.gate) : (shared ? a.sup : a.up);
       g.toff = a.tiles_gu;
       g.K = L->H;
       g.R = L->I;
-      g.act = a.xg;
-      g.act_scale = a.xdg;
+      g.act_hi = a.xhi;
+      g.act_lo = a.xlo;
     } else {
-      g.wa = shared ? a.sdown : a.down;
-      g.wb = g.wa;
+      g.w = shared ? a.sdown : a.down;
       g.toff = a.tiles_dn;
       g.K = L->I;
       g.R = L->H;
-      g.act = a.hbf;
-      g.act_scale = a.hd;
+      g.act_hi = a.hhi;
+      g.act_lo = a.hlo;
     }
-    g.dbg.trace = pass == 0 ? a.dbg.trace : nullptr;  // the timeline covers the routed gate/up GEMM
     if ((rc = tc_grouped_gemm(g, s))) return rc;
   }
   const size_t nout = static_cast<size_t>(T) * (L->H / 4);

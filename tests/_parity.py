@@ -62,7 +62,24 @@ def check_output(y_gpu, y_ref, bound, what=""):
     return worst, rel
 
 
-def check_token(L, cfg, x_row, y, g, partials):
+# Share of h elements whose int8 code may differ between the GPU's
+# quantization and the fp64 oracle's own (each side quantizes its own h; the
+# GPU's h is checked against the oracle's quantizer bit for bit regardless).
+# Decode and q=4 sum exact int32 block partials in fp32: 0.1 %. The prefill's
+# tensor-core operands carry code x scale to 16 significant bits (the part
+# below 2^-16 of each value is left out), so h differs from the oracle's by
+# up to ~3e-5 relative and ~0.2 % of the codes flip (measured): 1 %.
+FLIPS_DECODE = 1e-3
+FLIPS_PREFILL = 1e-2
+# Absolute tolerance of h, as a fraction of the token's max |h|: the left-out
+# operand bits give the prefill an error of up to ~2^-16 of sum |w x| per
+# output, i.e. a fixed fraction of the largest h rather than of each element.
+H_ATOL_DECODE = 2e-6
+H_ATOL_PREFILL = 1e-4
+PREFILL = dict(flip_frac=FLIPS_PREFILL, h_atol=H_ATOL_PREFILL)
+
+
+def check_token(L, cfg, x_row, y, g, partials, flip_frac=FLIPS_DECODE, h_atol=H_ATOL_DECODE):
     """Stage-by-stage parity of one token's decode intermediates g (one
     column's view of the debug buffers) and output y against the oracle.
     Returns the independent oracle output, the bound B and whether the GPU's
@@ -76,7 +93,7 @@ def check_token(L, cfg, x_row, y, g, partials):
     np.testing.assert_array_equal(g["idx"], tr["idx"])
     np.testing.assert_allclose(g["p"], tr["p"], rtol=2e-6)
     h = g["h"].reshape(ns, I)
-    np.testing.assert_allclose(h, tr["h"][:ns], rtol=2e-4, atol=2e-6 * np.abs(tr["h"][:ns]).max())
+    np.testing.assert_allclose(h, tr["h"][:ns], rtol=2e-4, atol=h_atol * np.abs(tr["h"][:ns]).max())
     # quantization decision: the oracle's quantizer on the GPU's h, bit for bit
     hq = g["hq"].reshape(ns, I)
     hd = g["hd"].reshape(ns, I // 32)
@@ -89,7 +106,7 @@ def check_token(L, cfg, x_row, y, g, partials):
         np.testing.assert_array_equal(hd[s], d)
     # independent quantization differs at most by one step, on rare elements
     diff = np.abs(hq.astype(int) - tr["hq"][:ns].astype(int))
-    assert diff.max() <= 1 and (diff > 0).sum() <= max(2, 1e-3 * diff.size)
+    assert diff.max() <= 1 and (diff > 0).sum() <= max(2, flip_frac * diff.size)
     # teacher-forced down projection: bit-exact partials, tight y
     yt, tt = O.ffn_decode(L, x_row, trace=True, partials=partials, force_hq=hq, force_hd=hd)
     if partials:

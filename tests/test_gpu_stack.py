@@ -20,7 +20,7 @@ import bit_codebook_quantized_dequant_gb300 as M
 from bit_codebook_quantized_dequant_gb300 import synth as S
 from bit_codebook_quantized_dequant_gb300.workload import (Debug, Workspace, build_layer,
                                                            to_dev_u16)
-from _parity import ELEM, REL_L2, check_token, column_view, host_layer_for
+from _parity import ELEM, PREFILL, REL_L2, check_token, column_view, host_layer_for
 
 pytestmark = pytest.mark.gpu
 
@@ -64,7 +64,7 @@ def test_stack_matches_composition_and_oracle():
         for i, t in enumerate(SAMPLE):
             np.testing.assert_array_equal(a_host[t], O.rmsnorm_bf16(r_host[t]))
             gt = column_view(g, cfg, t)
-            _, B, _ = check_token(L, cfg, a_host[t], y_host[t], gt, False)
+            _, B, _ = check_token(L, cfg, a_host[t], y_host[t], gt, False, **PREFILL)
             bounds[i] += B
             gpu_idx[l][i] = gt["idx"].copy()
             gpu_q[l][i] = (a_host[t].copy(), gt["xq"].copy(), gt["hq"].copy())
