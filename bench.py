@@ -65,6 +65,12 @@ def prefill_flops(cfg: dict, T: int) -> float:
     return 2.0 * T * ns * 3 * cfg["H"] * cfg["I"]
 
 
+def prefill_launches(cfg: dict) -> int:
+    """Kernels one moe_ffn_prefill call launches: route, prep_x, count, place,
+    gather, gate/up/down per routed and shared group, combine."""
+    return 5 + 3 * (2 if cfg["shared_fmt"] else 1) + 1
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -319,12 +325,16 @@ def bench_prefill(args, cid, T, tc_peak, hbm_peak, peak_kind):
            "ms_per_call": ms, "calls": steps, "tokens": T,
            "workload": S.CONFIGS[cid]["name"] + f": T={T}, all 256 experts' weights read once",
            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                        "frac": tflops / tc_peak, "traffic": None,
+                        "frac": tflops / tc_peak,
+                        "traffic": _traffic(f"prefill cfg{cid} gemm",
+                                            "bit_codebook_quantized_dequant_gb300/csrc/gemm_tc.cu"),
+                        "traffic_scope": "DRAM bytes of the gate, up and down tensor-core "
+                                         "launches of one call (routed experts)",
                         "peak_source": f"{peak_kind} bf16_tflops (the prefill contraction runs "
                                        "bf16-exact integer products)",
                         "algorithmic_flops_per_launch": fl,
                         "hbm_frac_weights": wbytes / (ms * 1e-3) / 1e9 / hbm_peak},
-           "gpu_launches_per_call": 10}
+           "gpu_launches_per_call": prefill_launches(cfg)}
     del dl, ws
     torch.cuda.empty_cache()
     return out
@@ -338,9 +348,9 @@ def run_sections(args, hbm_peak, tc_peak, peak_kind):
         out["verify_q4"] = bench_verify(args, hbm_peak, peak_kind)
     pre = []
     if "prefill" in sec or "prefill3" in sec:
-        pre.append(bench_prefill(args, 3, 2048, tc_peak, hbm_peak, peak_kind))
+        pre.append(bench_prefill(args, 3, args.prefill_tokens or 2048, tc_peak, hbm_peak, peak_kind))
     if "prefill" in sec or "prefill4" in sec:
-        pre.append(bench_prefill(args, 4, 32512, tc_peak, hbm_peak, peak_kind))
+        pre.append(bench_prefill(args, 4, args.prefill_tokens or 32512, tc_peak, hbm_peak, peak_kind))
     if pre:
         out["prefill"] = pre
     return out
@@ -487,6 +497,9 @@ def main():
     ap.add_argument("--sections", default="decode,verify,prefill",
                     help="comma list of decode, verify, prefill (= prefill3,prefill4); "
                          "without decode only the named sections run (profiling)")
+    ap.add_argument("--prefill-tokens", type=int, default=0,
+                    help="tokens of the prefill sections (default: the workloads' 2048 and 32512); "
+                         "smaller counts for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -1,35 +1,46 @@
 // Grouped GEMMs of the prefill on the 5th-generation tensor cores (tcgen05).
 //
-// One tile = 128 weight rows x 128 grouped rows (tokens of one expert), the
-// whole contraction K. The block scales are folded into the operands and the
-// operands split into bf16 parts so that every tensor-core product is exact:
+// One tile = 128 weight rows x up to 128 grouped rows (tokens of one expert),
+// the whole contraction K. The block scales are folded into the operands and
+// the operands split into bf16 parts:
 //   weights  a = cb[code] * ws[r, b]   (<= 19 significant bits, exact in fp32)
 //   activ.   x = q * d[t, b]            (<= 18 significant bits, exact in fp32)
 //   a = a_hi + a_lo, x = x_hi + x_lo with a_hi = bf16(a), a_lo = bf16(a - a_hi)
-//   (the part left out is below 2^-16 of the value; for power-of-two (E8M0)
-//   weight scales a is a bf16 value itself and a_lo = 0)
-// and a . x = sum of the part products, each exact in the fp32 accumulator.
-// tcgen05.mma kind::f16 accumulates the parts and all 32-element blocks of K
-// into one TMEM accumulator per tile, read out once per tile -- no per-block
+//   (what the two parts leave out is below 2^-18 of the value; for power-of-two
+//   (E8M0) weight scales a is a bf16 value itself and a_lo = 0)
+// and a . x = a_hi x_hi + a_hi x_lo + a_lo x_hi, each product exact in the fp32
+// accumulator; the term left out, a_lo x_lo, is below 2^-18 of |a x|.
+// tcgen05.mma kind::f16 accumulates the products and all 32-element blocks of
+// K into one TMEM accumulator per tile, read out once per tile -- no per-block
 // hand-off between the tensor cores and the CUDA cores. The only difference to
-// the per-block formulation is the order of the fp32 sums (and the parts' last
-// bits), well inside the FFN output tolerance.
+// the per-block formulation is the order of the fp32 sums and the parts' last
+// bits, well inside the FFN output tolerance.
+//
+// The expanded weights (operand A) never touch shared memory: the expansion
+// threads write them into TMEM (tcgen05.st, lane = weight row) and the MMA
+// reads A from TMEM, so shared memory only carries the activation tiles (B).
+// The MMA's N follows the rows a tile really has (a multiple of 16), so small
+// expert groups do not pay for a full 128-row tile.
 //
 // Three GEMMs per expert kind: gate (epilogue: g to memory), up (epilogue:
 // h = silu(g) u, H32 and Q8 of the 32-block of h, which is the 32 rows of one
 // warp, and h's parts for the down GEMM), down (epilogue: the fp32 rows).
 //
-// Warp roles (16 warps):
-//   0-3   expansion: thread = weight row; packed codes and block scales arrive
-//         by cp.async into a per-row buffer; per block the codebook scaled by
-//         the block scale is split into bf16 parts and looked up with byte
-//         permutes, written in the 128-byte-swizzled K-major operand layout
-//   4     activation producer: TMA (SWIZZLE_128B) of the tile's 128 grouped
-//         rows, parts hi and lo, 64 K-elements per stage
-//   5     MMA issuer (one thread) and TMEM owner
-//   8-15  epilogue: two warpgroups, 64 columns each, once per tile
-// Rings (mbarriers, every wait bounded): 2 operand stages, 2 TMEM tile
-// accumulators (the epilogue of one tile overlaps the next tile's main loop).
+// Warp roles (18 warps):
+//   0-7   expansion: warp w serves the rows of TMEM lane quarter w % 4 and the
+//         32-block w / 4 of each 64-element stage; its packed codes, the
+//         chunk's block scales and the tile's codebook arrive by cp.async into
+//         a per-thread buffer; per block the codebook scaled by the block scale
+//         is split into bf16 parts, looked up with byte permutes and stored
+//         into the stage's TMEM columns
+//   8     activation producer: TMA (SWIZZLE_128B) of the tile's grouped rows,
+//         parts hi and lo, 64 K-elements per stage, in 64-row boxes
+//   9     MMA issuer (one thread) and TMEM owner
+//   10-17 epilogue, two warps per TMEM lane quarter (64 columns each), once
+//         per tile
+// Rings (mbarriers, every wait bounded): 4 operand stages (B in shared memory,
+// A in TMEM), 2 TMEM tile accumulators (the epilogue of one tile overlaps the
+// next tile's main loop).
 //
 // Sources: "DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
 // 395", section "ROCmFPX: fitting 284B weights into 128 GB" (small codebooks
@@ -46,33 +57,42 @@
 namespace moeq {
 namespace {
 
-constexpr int kTM = 128;        // weight rows per tile
-constexpr int kTN = 128;        // grouped rows per tile
-constexpr int kKC = 8;          // 32-blocks per raw code chunk
-constexpr int kStages = 2;      // operand stages (64 K-elements each)
+constexpr int kTM = 128;        // weight rows per tile = TMEM lanes
+constexpr int kTN = 128;        // grouped rows per tile (largest MMA N)
+constexpr int kBoxRows = 64;    // grouped rows per TMA box
+constexpr int kKC = 8;          // 32-blocks per raw code chunk (4 stages)
+constexpr int kStages = 4;      // operand stages (64 K-elements each)
 constexpr int kAccBufs = 2;     // TMEM tile accumulators
-constexpr int kTcThreads = 512;
-constexpr int kBWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kEpiWarp0 = 8;
-constexpr uint32_t kTmemCols = kAccBufs * kTN;
+constexpr int kTcThreads = 576;
+constexpr int kExpWarps = 8;
+constexpr int kBWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEpiWarp0 = 10;
+constexpr int kEpiWarps = 8;     // two per TMEM lane quarter, 64 columns each
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcol0 = kAccBufs * kTN;  // first TMEM column of the weight ring
 
 template <int FMT>
 struct TcSmem {
   static constexpr int NA = FMT == 4 ? 1 : 2;  // weight parts
   static constexpr int BC = block_bytes<FMT>();
-  // raw row: the chunk's codes, then its block scales (<= 16 B); the pitch
-  // also keeps the rows of a warp on different banks
-  static constexpr int RP = kKC * BC + 16;
-  uint8_t a[kStages][NA][kTM * 128];  // weight parts: 128 rows x 64 bf16, SW128 K-major
+  // per-thread raw buffer: the codes of the thread's 4 blocks of a chunk, the
+  // chunk's block scales (<= 16 B), the tile's codebook (<= 16 B)
+  // (an odd number of 16-byte units, so that the threads of a quarter warp
+  // start on different banks)
+  static constexpr int RPT = ((kKC / 2) * BC + 32) / 16 % 2 ? (kKC / 2) * BC + 32 : (kKC / 2) * BC + 48;
+  static constexpr int SCL = (kKC / 2) * BC;
+  static constexpr int CBO = SCL + 16;
   uint8_t b[kStages][2][kTN * 128];   // activation parts: 128 rows x 64 bf16, SW128 K-major
-  uint8_t raw[2][kTM][RP];            // packed code chunks [stage][row]
+  uint8_t raw[2][kExpWarps * 32][RPT];
   uint64_t full[kStages], empty[kStages];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;                     // completion of every MMA this CTA issued
+  uint32_t nmma[kStages];             // MMA N of the stage (its tile's rows, rounded up to 16)
   uint32_t tmem_base;
   volatile int abort;
 };
+static_assert(kAcol0 + kStages * 2 * 32 <= kTmemCols, "TMEM: accumulators + weight ring");
 
 enum EpiKind { EPI_G = 0, EPI_SWIGLU = 1, EPI_O = 2 };
 
@@ -103,13 +123,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return d;
 }
 
-// kind::f16, bf16 A and B, fp32 D, both K-major, M = 128, N = kTN.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kTN >> 3) << 17) | ((kTM >> 4) << 24);
+// kind::f16, bf16 A and B, fp32 D, both K-major, M = 128; N (a multiple of 16) at bits 17..22.
+constexpr uint32_t kIdescM = (1u << 4) | (1u << 7) | (1u << 10) | ((kTM >> 4) << 24);
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t accumulate) {
+// D[tmem] (+)= A[TMEM, lane = row, bf16 pairs along the columns] x B[smem descriptor]^T
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-               :: "r"(d_tmem), "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate));
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(bd), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -126,6 +148,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// 16 columns of this warp's lane quarter from 16 registers per thread.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                  "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -173,13 +204,11 @@ __device__ __forceinline__ bool ring_wait(TcSmem<FMT>& sm, uint64_t* bar, uint32
   return false;
 }
 
-// Warp-wide form: lane 0 waits, the result is broadcast.
+// Warp-wide form: every lane polls the barrier (one broadcast read), the
+// decision is made uniform across the warp.
 template <int FMT>
-__device__ __forceinline__ bool warp_wait(TcSmem<FMT>& sm, uint64_t* bar, uint32_t parity, int32_t* status,
-                                          int lane) {
-  bool ok = true;
-  if (lane == 0) ok = ring_wait<FMT>(sm, bar, parity, status);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+__device__ __forceinline__ bool warp_wait(TcSmem<FMT>& sm, uint64_t* bar, uint32_t parity, int32_t* status) {
+  return __all_sync(0xffffffffu, ring_wait<FMT>(sm, bar, parity, status) ? 1 : 0) != 0;
 }
 
 // ---------------------------------------------------------------- operand parts
@@ -232,51 +261,51 @@ __device__ __forceinline__ void interleave4(uint32_t lo, uint32_t hi, uint32_t* 
   out[1] = prmt(lo, hi, 0x7362u);
 }
 
-// One block (32 codes at p) -> 16 words of bf16 pairs (elements 2i, 2i+1 in
+// The packed codes of one block (BC bytes at p, 8- or 16-byte aligned for
+// FP2 / FP4, 4-byte for FP3) into registers.
+template <int FMT>
+__device__ __forceinline__ void load_codes(const uint8_t* p, uint32_t (&w)[4]) {
+  if constexpr (FMT == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = 0; w[3] = 0;
+  } else if constexpr (FMT == 3) {
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
+    w[0] = q[0]; w[1] = q[1]; w[2] = q[2]; w[3] = 0;
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  }
+}
+
+// One block (its code words w) -> 16 words of bf16 pairs (elements 2i, 2i+1 in
 // word i), values from the byte planes tl (low bytes) and th (high bytes).
 template <int FMT>
-__device__ __forceinline__ void expand_bf16(const uint8_t* p, const uint32_t* tl, const uint32_t* th,
+__device__ __forceinline__ void expand_bf16(const uint32_t (&w)[4], const uint32_t* tl, const uint32_t* th,
                                             uint32_t* out) {
   if constexpr (FMT == 2) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-    const uint32_t ws[2] = {w.x, w.y};
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const uint32_t sa = ws[q] & 0x33333333u, sb = (ws[q] >> 2) & 0x33333333u;
+      const uint32_t sa = w[q] & 0x33333333u, sb = (w[q] >> 2) & 0x33333333u;
       const uint32_t sel[4] = {sa, sa >> 16, sb, sb >> 16};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         interleave4(prmt(tl[0], tl[0], sel[i]), prmt(th[0], th[0], sel[i]), out + 8 * q + 2 * i);
     }
   } else if constexpr (FMT == 3) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
     const Fp3Sel s = fp3_selectors(w[0], w[1], w[2]);
     const uint32_t sel[8] = {s.s00, s.s00 >> 16, s.s01, s.s01 >> 16, s.s10, s.s10 >> 16, s.s11, s.s11 >> 16};
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       interleave4(prmt(tl[0], tl[1], sel[i]), prmt(th[0], th[1], sel[i]), out + 2 * i);
   } else {
-    const uint4 wd = *reinterpret_cast<const uint4*>(p);
-    const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint32_t l0, l1, h0, h1;
-      fp4_expand(ws[q], tl[0], tl[1], tl[2], tl[3], l0, l1);
-      fp4_expand(ws[q], th[0], th[1], th[2], th[3], h0, h1);
+      fp4_expand(w[q], tl[0], tl[1], tl[2], tl[3], l0, l1);
+      fp4_expand(w[q], th[0], th[1], th[2], th[3], h0, h1);
       interleave4(l0, h0, out + 4 * q);
       interleave4(l1, h1, out + 4 * q + 2);
     }
-  }
-}
-
-// Writes a block's 16 words (32 bf16, K-elements 32 hb .. 32 hb + 31 of the
-// stage) into row r of a 128-byte-swizzled K-major operand tile.
-__device__ __forceinline__ void put_row(uint8_t* tile, int r, int hb, const uint32_t* v) {
-  uint8_t* rowp = tile + r * 128;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int ch = (4 * hb + i) ^ (r & 7);
-    *reinterpret_cast<uint4*>(rowp + 16 * ch) = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
   }
 }
 
@@ -284,22 +313,30 @@ struct TileInfo {
   int g, e, m0, tt, off, n;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const TcArgs& a, int tile) {
-  int lo = a.g0, hi = a.g1 - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&a.toff[mid]) <= tile) lo = mid;
-    else hi = mid - 1;
+// Group of `tile`, scanning forward from group g, the group of an earlier tile
+// of this CTA (tiles are numbered group by group; toff[c] = first tile of group
+// c, non-decreasing, so the groups with toff[c] <= tile form a prefix). All 32
+// lanes call it; one load per lane and step of 32 groups.
+__device__ __forceinline__ int group_from(const TcArgs& a, int tile, int g, int lane) {
+  for (;;) {
+    const int c = g + 1 + lane;
+    const bool le = c < a.g1 && __ldg(&a.toff[c]) <= tile;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    g += __popc(m);
+    if (m != 0xffffffffu) return g;
   }
+}
+
+__device__ __forceinline__ TileInfo tile_at(const TcArgs& a, int tile, int g) {
   TileInfo t;
-  t.g = lo;
-  const int local = tile - __ldg(&a.toff[lo]);
+  t.g = g;
+  const int local = tile - __ldg(&a.toff[g]);
   const int rtiles = a.R / kTM;
   t.tt = local / rtiles;
   t.m0 = (local % rtiles) * kTM;
-  t.e = a.shared ? 0 : lo;
-  t.off = __ldg(&a.offsets[lo]);
-  t.n = __ldg(&a.offsets[lo + 1]) - t.off;
+  t.e = a.shared ? 0 : g;
+  t.off = __ldg(&a.offsets[g]);
+  t.n = __ldg(&a.offsets[g + 1]) - t.off;
   return t;
 }
 
@@ -314,6 +351,12 @@ __device__ __forceinline__ void pid_split(const TcArgs& a, int pid, int& t, int&
   }
 }
 
+// TMEM column of the weight ring: stage slot, part pa.
+template <int NA>
+__device__ __forceinline__ uint32_t a_col(int slot, int pa) {
+  return kAcol0 + static_cast<uint32_t>((slot * NA + pa) * 32);
+}
+
 // ---------------------------------------------------------------- kernel
 template <int FMT, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_hi,
@@ -322,8 +365,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   TcSmem<FMT>& sm = *reinterpret_cast<TcSmem<FMT>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr int BC = block_bytes<FMT>();
-  constexpr int NA = TcSmem<FMT>::NA;
+  using SM = TcSmem<FMT>;
+  constexpr int BC = SM::BC;
+  constexpr int NA = SM::NA;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = a.K / 32;
   const int nstages = a.K / 64;
@@ -332,12 +376,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm.full[i], 5);   // 4 expansion warps + the activation producer (+ its bytes)
-      mbar_init(&sm.empty[i], 1);  // MMA commit
+      mbar_init(&sm.full[i], kExpWarps + 1);  // expansion warps + the activation producer (+ its bytes)
+      mbar_init(&sm.empty[i], 1);             // MMA commit
     }
     for (int i = 0; i < kAccBufs; ++i) {
-      mbar_init(&sm.acc_full[i], 1);   // MMA commit
-      mbar_init(&sm.acc_empty[i], 8);  // epilogue warps
+      mbar_init(&sm.acc_full[i], 1);  // MMA commit
+      mbar_init(&sm.acc_empty[i], kEpiWarps);
     }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -345,7 +389,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(&sm.tmem_base)), "r"(kTmemCols));
+                 :: "r"(smem_u32(&sm.tmem_base)), "n"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -353,89 +397,130 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp < 4) {
-    // ------------------------------------------------------------ expansion (thread = row)
-    const int r = tid;
-    int ks = 0;
+  if (warp < kExpWarps) {
+    // ------------------------------------------------------------ expansion
+    const int q = warp & 3, hb = warp >> 2;
+    const int r = 32 * q + lane;                       // weight row in the tile = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
     constexpr int NV = 1 << FMT;
-    for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
-      const TileInfo t = tile_info(a, t_begin + ti);
-      float cbf[NV];
-      const int8_t* cb = a.w.cb + static_cast<size_t>(t.e) * a.w.cb_stride;
-#pragma unroll
-      for (int v = 0; v < NV; ++v) cbf[v] = static_cast<float>(cb[v]);
+    constexpr int SB = FMT == 4 ? 1 : 2;
+    // chunk c of tile t into raw buffer `buf`: this thread's blocks (kc + 2j + hb),
+    // the chunk's scales, for c = 0 the tile's codebook
+    auto issue_chunk = [&](const TileInfo& t, int c, int buf) {
       const size_t row = static_cast<size_t>(t.m0 + r);
-      // one chunk of the row: its codes and its block scales, by asynchronous copies
-      auto issue_chunk = [&](int c) {
-        constexpr int SB = FMT == 4 ? 1 : 2;
-        const int kc = c * kKC, kb = min(kKC, nb - kc);
-        const uint8_t* src = a.w.codes + static_cast<size_t>(t.e) * a.w.stride_codes + (row * nb + kc) * BC;
-        uint8_t* dst = sm.raw[c & 1][r];
-        for (int i = 0; i < kb * BC / 16; ++i) cp_async16(dst + 16 * i, src + 16 * i);
-        const size_t soff = (row * nb + kc) * SB;
-        const uint8_t* ssrc = a.w.scales + static_cast<size_t>(t.e) * a.w.stride_scales + soff;
-        uint8_t* sdst = dst + kKC * BC;
-        const int sbytes = kb * SB;  // 4, 8 or 16; soff is aligned to the piece used
-        if (sbytes % 16 == 0 && soff % 16 == 0) {
-          for (int i = 0; i < sbytes; i += 16) cp_async16(sdst + i, ssrc + i);
-        } else if (sbytes % 8 == 0 && soff % 8 == 0) {
-          for (int i = 0; i < sbytes; i += 8) cp_async8(sdst + i, ssrc + i);
+      const int kc = c * kKC, kb = min(kKC, nb - kc);
+      uint8_t* dst = sm.raw[buf][tid];
+      const uint8_t* src = a.w.codes + static_cast<size_t>(t.e) * a.w.stride_codes + (row * nb + kc) * BC;
+      for (int j = 0; j < kb / 2; ++j) {
+        const uint8_t* bs = src + (2 * j + hb) * BC;
+        if constexpr (FMT == 2) {
+          cp_async8(dst + j * BC, bs);
+        } else if constexpr (FMT == 3) {
+          cp_async4(dst + j * BC, bs);
+          cp_async4(dst + j * BC + 4, bs + 4);
+          cp_async4(dst + j * BC + 8, bs + 8);
         } else {
-          for (int i = 0; i < sbytes; i += 4) cp_async4(sdst + i, ssrc + i);
+          cp_async16(dst + j * BC, bs);
         }
-        cp_async_commit();
-      };
-      const int nchunks = (nb + kKC - 1) / kKC;
-      issue_chunk(0);
-      for (int c = 0; c < nchunks; ++c) {
+      }
+      const size_t soff = (row * nb + kc) * SB;
+      const uint8_t* ssrc = a.w.scales + static_cast<size_t>(t.e) * a.w.stride_scales + soff;
+      uint8_t* sdst = dst + SM::SCL;
+      const int sbytes = kb * SB;  // 4, 8 or 16; soff is aligned to the piece used
+      if (sbytes % 16 == 0 && soff % 16 == 0) {
+        for (int i = 0; i < sbytes; i += 16) cp_async16(sdst + i, ssrc + i);
+      } else if (sbytes % 8 == 0 && soff % 8 == 0) {
+        for (int i = 0; i < sbytes; i += 8) cp_async8(sdst + i, ssrc + i);
+      } else {
+        for (int i = 0; i < sbytes; i += 4) cp_async4(sdst + i, ssrc + i);
+      }
+      if (c == 0) {  // codebook record: 16-byte aligned, NV bytes
+        const int8_t* cb = a.w.cb + static_cast<size_t>(t.e) * a.w.cb_stride;
+        if constexpr (NV == 16) cp_async16(dst + SM::CBO, cb);
+        else if constexpr (NV == 8) cp_async8(dst + SM::CBO, cb);
+        else cp_async4(dst + SM::CBO, cb);
+      }
+      cp_async_commit();
+    };
+    const int nchunks = (nb + kKC - 1) / kKC;
+    int ti = blockIdx.x, g = a.g0, cg = 0, ks = 0;
+    TileInfo cur{};
+    if (ti < ntiles) {
+      g = group_from(a, t_begin + ti, g, lane);
+      cur = tile_at(a, t_begin + ti, g);
+      issue_chunk(cur, 0, 0);
+    }
+    float cbf[NV];
+    for (; ti < ntiles && !sm.abort; ti += gridDim.x) {
+      const int tn = ti + gridDim.x;
+      const bool has_next = tn < ntiles;
+      TileInfo nxt{};
+      if (has_next) {
+        g = group_from(a, t_begin + tn, g, lane);
+        nxt = tile_at(a, t_begin + tn, g);
+      }
+      for (int c = 0; c < nchunks; ++c, ++cg) {
         if (c + 1 < nchunks) {
-          issue_chunk(c + 1);
+          issue_chunk(cur, c + 1, (cg + 1) & 1);
+          cp_async_wait<1>();
+        } else if (has_next) {
+          issue_chunk(nxt, 0, (cg + 1) & 1);
           cp_async_wait<1>();
         } else {
           cp_async_wait<0>();
         }
-        const int kc = c * kKC, kb = min(kKC, nb - kc);
-        const uint8_t* rawr = sm.raw[c & 1][r];
+        const uint8_t* rawr = sm.raw[cg & 1][tid];
+        if (c == 0) {
+#pragma unroll
+          for (int v = 0; v < NV; ++v) cbf[v] = static_cast<float>(reinterpret_cast<const int8_t*>(rawr + SM::CBO)[v]);
+        }
+        const int kb = min(kKC, nb - c * kKC);
         for (int jp = 0; jp < kb / 2; ++jp, ++ks) {
           const int slot = ks % kStages;
-          if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status, lane)) break;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const int jb = 2 * jp + hb;
-            float ws;
-            if constexpr (FMT == 4) ws = e8m0_to_f32(rawr[kKC * BC + jb]);
-            else ws = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(rawr + kKC * BC)[jb]);
-            uint32_t tl[4], th[4], ul[4], uh[4];
-            scaled_tables<FMT>(cbf, ws, tl, th, ul, uh);
-            uint32_t v[16];
-            expand_bf16<FMT>(rawr + jb * BC, tl, th, v);
-            put_row(sm.a[slot][0], r, hb, v);
-            if constexpr (NA == 2) {
-              expand_bf16<FMT>(rawr + jb * BC, ul, uh, v);
-              put_row(sm.a[slot][NA - 1], r, hb, v);
-            }
-          }
-          fence_proxy_async();
+          if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status)) break;
+          const int jb = 2 * jp + hb;  // block in the chunk
+          float ws;
+          if constexpr (FMT == 4) ws = e8m0_to_f32(rawr[SM::SCL + jb]);
+          else ws = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(rawr + SM::SCL)[jb]);
+          uint32_t cw[4];
+          load_codes<FMT>(rawr + jp * BC, cw);
+          uint32_t tl[4], th[4], ul[4], uh[4];
+          scaled_tables<FMT>(cbf, ws, tl, th, ul, uh);
+          uint32_t vh[16], vl[16];
+          expand_bf16<FMT>(cw, tl, th, vh);
+          if constexpr (NA == 2) expand_bf16<FMT>(cw, ul, uh, vl);
+          tmem_st16(lane_base + a_col<NA>(slot, 0) + 16 * hb, vh);
+          if constexpr (NA == 2) tmem_st16(lane_base + a_col<NA>(slot, 1) + 16 * hb, vl);
+          tmem_wait_st();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.full[slot]);
         }
         if (sm.abort) break;
       }
+      cur = nxt;
     }
     cp_async_wait<0>();
   } else if (warp == kBWarp) {
     // ------------------------------------------------------------ activation producer
-    int ks = 0;
+    int ks = 0, g = a.g0;
     for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
-      const TileInfo t = tile_info(a, t_begin + ti);
+      g = group_from(a, t_begin + ti, g, lane);
+      const TileInfo t = tile_at(a, t_begin + ti, g);
       const int y0 = t.off + t.tt * kTN;
+      const int nv = min(kTN, t.n - t.tt * kTN);          // >= 1
+      const int nbox = (nv + kBoxRows - 1) / kBoxRows;
+      const uint32_t nm = static_cast<uint32_t>(min(kTN, (nv + 15) & ~15));
       for (int p = 0; p < nstages; ++p, ++ks) {
         const int slot = ks % kStages;
-        if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status, lane)) break;
+        if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.full[slot], 2 * kTN * 128);
-          tma_load_2d(sm.b[slot][0], &tm_hi, 64 * p, y0, &sm.full[slot]);
-          tma_load_2d(sm.b[slot][1], &tm_lo, 64 * p, y0, &sm.full[slot]);
+          sm.nmma[slot] = nm;
+          mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(2 * nbox * kBoxRows * 128));
+          for (int bx = 0; bx < nbox; ++bx) {
+            tma_load_2d(sm.b[slot][0] + bx * kBoxRows * 128, &tm_hi, 64 * p, y0 + bx * kBoxRows, &sm.full[slot]);
+            tma_load_2d(sm.b[slot][1] + bx * kBoxRows * 128, &tm_lo, 64 * p, y0 + bx * kBoxRows, &sm.full[slot]);
+          }
         }
         __syncwarp();
       }
@@ -443,6 +528,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
+      // descriptor of b[slot][pb]: the parts are 16 KB apart, 1024 in the address field (addr >> 4)
+      const uint64_t bdesc0 = sw128_desc(smem_u32(sm.b[0][0]));
+      static_assert(sizeof(sm.b[0][0]) == 16384, "B part size");
       int ks = 0, kt = 0;
       bool ok = true;
       for (int ti = blockIdx.x; ti < ntiles && ok; ti += gridDim.x, ++kt) {
@@ -455,16 +543,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
           const int slot = ks % kStages;
           if (!(ok = ring_wait<FMT>(sm, &sm.full[slot], (ks / kStages) & 1, a.status))) break;
           tc_fence_after();
+          const uint32_t idesc = kIdescM | ((sm.nmma[slot] >> 3) << 17);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t koff = static_cast<uint32_t>(kk * 32);
+            // products a_hi x_hi, a_hi x_lo (and a_lo x_hi for two weight parts)
 #pragma unroll
-            for (int pa = 0; pa < NA; ++pa)
-#pragma unroll
-              for (int pb = 0; pb < 2; ++pb)
-                mma_bf16(dcol, sw128_desc(smem_u32(sm.a[slot][pa]) + koff),
-                         sw128_desc(smem_u32(sm.b[slot][pb]) + koff),
-                         (p > 0 || kk > 0 || pa > 0 || pb > 0) ? 1u : 0u);
+            for (int pr = 0; pr < NA + 1; ++pr) {
+              const int pa = pr == 2 ? 1 : 0, pb = pr == 1 ? 1 : 0;
+              const uint64_t bd = bdesc0 + static_cast<uint64_t>((2 * slot + pb) * 1024 + 2 * kk);
+              mma_bf16_ts(dcol, tmem + a_col<NA>(slot, pa) + 8 * kk, bd, idesc,
+                          (p > 0 || kk > 0 || pr > 0) ? 1u : 0u);
+            }
           }
           mma_commit(&sm.empty[slot]);
         }
@@ -481,61 +570,74 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue (once per tile)
     const int q = warp & 3;                // TMEM lane quarter = rows 32q .. 32q + 31
-    const int c0 = 64 * ((warp - kEpiWarp0) >> 2);  // this warpgroup's 64 columns
+    const int half = (warp - kEpiWarp0) >> 2;  // columns 64 half .. 64 half + 63
     const int r = 32 * q + lane;
-    int kt = 0;
+    int kt = 0, g = a.g0;
     for (int ti = blockIdx.x; ti < ntiles; ti += gridDim.x, ++kt) {
-      const TileInfo t = tile_info(a, t_begin + ti);
+      g = group_from(a, t_begin + ti, g, lane);
+      const TileInfo t = tile_at(a, t_begin + ti, g);
       const int tb = kt % kAccBufs;
-      if (!warp_wait<FMT>(sm, &sm.acc_full[tb], (kt / kAccBufs) & 1, a.status, lane)) break;
+      if (!warp_wait<FMT>(sm, &sm.acc_full[tb], (kt / kAccBufs) & 1, a.status)) break;
       tc_fence_after();
-      float acc[64];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * kTN + c0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tmem_ld16(taddr + 16 * i, acc + 16 * i);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acc_empty[tb]);
+      const int nv = min(kTN, t.n - t.tt * kTN);
       const size_t rowcol = static_cast<size_t>(t.m0 + r);
+      constexpr int CW = EPI == EPI_SWIGLU ? 16 : 32;  // columns per TMEM read
+      for (int c0 = 64 * half; c0 < min(nv, 64 * half + 64); c0 += CW) {
+        float acc[CW];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(tb * kTN + c0);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const int jr = t.tt * kTN + c0 + j;
-        if (jr >= t.n) continue;  // warp-uniform
-        const size_t grow = static_cast<size_t>(t.off + jr);
-        const size_t at = grow * a.R + rowcol;
-        if constexpr (EPI == EPI_G) {
-          a.g[at] = acc[j];
-        } else if constexpr (EPI == EPI_O) {
-          a.o[at] = acc[j];
-          if (a.dbg.o) {
-            int tk, s;
-            pid_split(a, a.pid[grow], tk, s);
-            a.dbg.o[(static_cast<size_t>(tk) * a.ns + s) * a.R + rowcol] = acc[j];
+        for (int i = 0; i < CW; i += 16) tmem_ld16(taddr + i, acc + i);
+        tmem_wait_ld();
+        float gpre[EPI == EPI_SWIGLU ? CW : 1];
+        if constexpr (EPI == EPI_SWIGLU) {  // the chunk's g values first: independent loads in flight
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            const int jr = t.tt * kTN + c0 + j;
+            gpre[j] = jr < t.n ? __ldcg(&a.g[static_cast<size_t>(t.off + jr) * a.R + rowcol]) : 0.0f;
           }
-        } else {
-          const float gv = __ldcg(&a.g[at]), u = acc[j];
-          const float h = gv * u / (1.0f + expf(-gv));
-          const int blk = (t.m0 + 32 * q) / 32;
-          float vv = h;
-          if (a.signs_h) vv = h32_warp(vv, __ldg(&a.signs_h[blk]), lane);
-          uint16_t db;
-          const int8_t qv = q8_warp(vv, db);
-          // h's parts for the down GEMM: q * d (exact in fp32) as bf16 hi + lo
-          const float pv = __fmul_rn(static_cast<float>(qv), f16_bits_to_f32(db));
-          const uint32_t hp = bf16x2_rn(pv, 0.0f);
-          a.hhi[at] = static_cast<uint16_t>(hp & 0xffffu);
-          a.hlo[at] = static_cast<uint16_t>(bf16x2_rn(__fsub_rn(pv, bf16_lo_f(hp)), 0.0f) & 0xffffu);
-          if (a.dbg.h || a.dbg.hq || a.dbg.hd) {
-            int tk, s;
-            pid_split(a, a.pid[grow], tk, s);
-            const size_t vec = static_cast<size_t>(tk) * a.ns + s;
-            if (a.dbg.h) a.dbg.h[vec * a.R + rowcol] = h;
-            if (a.dbg.hq) a.dbg.hq[vec * a.R + rowcol] = qv;
-            if (a.dbg.hd && lane == 0) a.dbg.hd[vec * (a.R / 32) + blk] = db;
+        }
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          const int jr = t.tt * kTN + c0 + j;
+          if (jr >= t.n) continue;  // warp-uniform
+          const size_t grow = static_cast<size_t>(t.off + jr);
+          const size_t at = grow * a.R + rowcol;
+          if constexpr (EPI == EPI_G) {
+            a.g[at] = acc[j];
+          } else if constexpr (EPI == EPI_O) {
+            a.o[at] = acc[j];
+            if (a.dbg.o) {
+              int tk, s;
+              pid_split(a, a.pid[grow], tk, s);
+              a.dbg.o[(static_cast<size_t>(tk) * a.ns + s) * a.R + rowcol] = acc[j];
+            }
+          } else {
+            const float gv = gpre[j], u = acc[j];
+            const float h = gv * u / (1.0f + expf(-gv));
+            const int blk = (t.m0 + 32 * q) / 32;
+            float vv = h;
+            if (a.signs_h) vv = h32_warp(vv, __ldg(&a.signs_h[blk]), lane);
+            uint16_t db;
+            const int8_t qv = q8_warp(vv, db);
+            // h's parts for the down GEMM: q * d (exact in fp32) as bf16 hi + lo
+            const float pv = __fmul_rn(static_cast<float>(qv), f16_bits_to_f32(db));
+            const uint32_t hp = bf16x2_rn(pv, 0.0f);
+            a.hhi[at] = static_cast<uint16_t>(hp & 0xffffu);
+            a.hlo[at] = static_cast<uint16_t>(bf16x2_rn(__fsub_rn(pv, bf16_lo_f(hp)), 0.0f) & 0xffffu);
+            if (a.dbg.h || a.dbg.hq || a.dbg.hd) {
+              int tk, s;
+              pid_split(a, a.pid[grow], tk, s);
+              const size_t vec = static_cast<size_t>(tk) * a.ns + s;
+              if (a.dbg.h) a.dbg.h[vec * a.R + rowcol] = h;
+              if (a.dbg.hq) a.dbg.hq[vec * a.R + rowcol] = qv;
+              if (a.dbg.hd && lane == 0) a.dbg.hd[vec * (a.R / 32) + blk] = db;
+            }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[tb]);
     }
   }
 
@@ -544,7 +646,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "n"(kTmemCols));
   }
 }
 
@@ -567,11 +669,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 [rows x K] activation parts, boxes of 64 K-elements x 128 rows, 128-byte swizzle.
+// bf16 [rows x K] activation parts, boxes of 64 K-elements x 64 rows, 128-byte swizzle.
 int act_map(EncodeTiledFn enc, CUtensorMap* tm, const uint16_t* base, int K, int rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {64, kTN};
+  const cuuint32_t box[2] = {64, kBoxRows};
   const cuuint32_t es[2] = {1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -76,10 +76,17 @@ FLIPS_PREFILL = 1e-2
 # output, i.e. a fixed fraction of the largest h rather than of each element.
 H_ATOL_DECODE = 2e-6
 H_ATOL_PREFILL = 1e-4
-PREFILL = dict(flip_frac=FLIPS_PREFILL, h_atol=H_ATOL_PREFILL)
+# Per-slot output o against the oracle's, as a fraction of the slot's bound
+# sum |w x|: the decode's block sums are exact integers (fp32 rounding only);
+# the prefill's tensor-core operands leave out three pieces of at most 2^-18 of
+# |w x| each per product (the two split residuals and the low x low product).
+O_REL_DECODE = 1e-5
+O_REL_PREFILL = 2e-5
+PREFILL = dict(flip_frac=FLIPS_PREFILL, h_atol=H_ATOL_PREFILL, o_rel=O_REL_PREFILL)
 
 
-def check_token(L, cfg, x_row, y, g, partials, flip_frac=FLIPS_DECODE, h_atol=H_ATOL_DECODE):
+def check_token(L, cfg, x_row, y, g, partials, flip_frac=FLIPS_DECODE, h_atol=H_ATOL_DECODE,
+                o_rel=O_REL_DECODE):
     """Stage-by-stage parity of one token's decode intermediates g (one
     column's view of the debug buffers) and output y against the oracle.
     Returns the independent oracle output, the bound B and whether the GPU's
@@ -116,7 +123,8 @@ def check_token(L, cfg, x_row, y, g, partials, flip_frac=FLIPS_DECODE, h_atol=H_
     B = output_bound(L, tr["idx"], tr["p"], hq, hd)
     o = g["o"].reshape(ns, H)
     for s, bs in enumerate(slot_bounds(L, tr["idx"], hq, hd)):
-        assert np.all(np.abs(o[s] - tt["o"][s]) <= 1e-5 * bs), f"o[{s}]"
+        err = np.abs(o[s] - tt["o"][s])
+        assert np.all(err <= o_rel * bs), f"o[{s}]: max err/bound {np.max(err / bs):.3g}"
     check_output(y, yt, B, "y (teacher-forced)")
     same_q = np.array_equal(hq, tr["hq"][:ns]) and np.array_equal(hd, tr["hd"][:ns])
     return yo, B, same_q
