@@ -27,12 +27,13 @@
 // warp, and h's parts for the down GEMM), down (epilogue: the fp32 rows).
 //
 // Warp roles (18 warps):
-//   0-7   expansion: warp w serves the rows of TMEM lane quarter w % 4 and the
-//         32-block w / 4 of each 64-element stage; its packed codes, the
-//         chunk's block scales and the tile's codebook arrive by cp.async into
-//         a per-thread buffer; per block the codebook scaled by the block scale
-//         is split into bf16 parts, looked up with byte permutes and stored
-//         into the stage's TMEM columns
+//   0-7   expansion: warp w serves the rows of TMEM lane quarter w % 4 and
+//         the 64-element stages of parity w / 4; the packed codes of its
+//         stages, the chunk's block scales and the tile's codebook arrive by
+//         cp.async into a per-thread ring of 3 chunk buffers (2 chunks ahead);
+//         per block the codebook scaled by the block scale is split into bf16
+//         parts, looked up with byte permutes and stored into the stage's
+//         TMEM columns
 //   8     activation producer: TMA (SWIZZLE_128B) of the tile's grouped rows,
 //         parts hi and lo, 64 K-elements per stage, in 64-row boxes
 //   9     MMA issuer (one thread) and TMEM owner
@@ -63,6 +64,7 @@ constexpr int kBoxRows = 64;    // grouped rows per TMA box
 constexpr int kKC = 8;          // 32-blocks per raw code chunk (4 stages)
 constexpr int kStages = 4;      // operand stages (64 K-elements each)
 constexpr int kAccBufs = 2;     // TMEM tile accumulators
+constexpr int kRawBufs = 3;     // per-thread code chunk buffers (2 chunks prefetched)
 constexpr int kTcThreads = 576;
 constexpr int kExpWarps = 8;
 constexpr int kBWarp = 8;
@@ -84,7 +86,7 @@ struct TcSmem {
   static constexpr int SCL = (kKC / 2) * BC;
   static constexpr int CBO = SCL + 16;
   uint8_t b[kStages][2][kTN * 128];   // activation parts: 128 rows x 64 bf16, SW128 K-major
-  uint8_t raw[2][kExpWarps * 32][RPT];
+  uint8_t raw[kRawBufs][kExpWarps * 32][RPT];
   uint64_t full[kStages], empty[kStages];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;                     // completion of every MMA this CTA issued
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm.full[i], kExpWarps + 1);  // expansion warps + the activation producer (+ its bytes)
+      mbar_init(&sm.full[i], 5);  // the 4 expansion warps of the stage's parity + the activation producer (+ its bytes)
       mbar_init(&sm.empty[i], 1);             // MMA commit
     }
     for (int i = 0; i < kAccBufs; ++i) {
@@ -399,28 +401,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
   if (warp < kExpWarps) {
     // ------------------------------------------------------------ expansion
+    // warp (q, hb): rows 32q .. 32q + 31 of the tile, the stages of parity hb
+    // (every tile has an even number of stages, so the parity is the same in
+    // the tile and in the ring); both 32-blocks of each of its stages
     const int q = warp & 3, hb = warp >> 2;
     const int r = 32 * q + lane;                       // weight row in the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
     constexpr int NV = 1 << FMT;
     constexpr int SB = FMT == 4 ? 1 : 2;
-    // chunk c of tile t into raw buffer `buf`: this thread's blocks (kc + 2j + hb),
-    // the chunk's scales, for c = 0 the tile's codebook
+    const int nchunks = (nstages + 3) / 4;             // chunks of 4 stages = kKC blocks
+    // chunk c of tile t into raw buffer `buf`: the block pairs of this warp's
+    // stages (hb and hb + 2 of the chunk), the chunk's scales, for c = 0 the
+    // tile's codebook; the caller commits the group
     auto issue_chunk = [&](const TileInfo& t, int c, int buf) {
       const size_t row = static_cast<size_t>(t.m0 + r);
       const int kc = c * kKC, kb = min(kKC, nb - kc);
       uint8_t* dst = sm.raw[buf][tid];
       const uint8_t* src = a.w.codes + static_cast<size_t>(t.e) * a.w.stride_codes + (row * nb + kc) * BC;
-      for (int j = 0; j < kb / 2; ++j) {
-        const uint8_t* bs = src + (2 * j + hb) * BC;
-        if constexpr (FMT == 2) {
-          cp_async8(dst + j * BC, bs);
-        } else if constexpr (FMT == 3) {
-          cp_async4(dst + j * BC, bs);
-          cp_async4(dst + j * BC + 4, bs + 4);
-          cp_async4(dst + j * BC + 8, bs + 8);
+      for (int pp = 0; pp < 2; ++pp) {
+        const int sl = hb + 2 * pp;                    // stage in the chunk
+        if (2 * sl >= kb) break;
+        const uint8_t* ps = src + 2 * sl * BC;         // blocks 2 sl, 2 sl + 1: 2 BC contiguous bytes
+        uint8_t* pd = dst + 2 * pp * BC;
+        if constexpr (FMT == 3) {
+          cp_async8(pd, ps);
+          cp_async8(pd + 8, ps + 8);
+          cp_async8(pd + 16, ps + 16);
         } else {
-          cp_async16(dst + j * BC, bs);
+#pragma unroll
+          for (int i = 0; i < 2 * BC; i += 16) cp_async16(pd + i, ps + i);
         }
       }
       const size_t soff = (row * nb + kc) * SB;
@@ -440,65 +449,73 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         else if constexpr (NV == 8) cp_async8(dst + SM::CBO, cb);
         else cp_async4(dst + SM::CBO, cb);
       }
-      cp_async_commit();
     };
-    const int nchunks = (nb + kKC - 1) / kKC;
-    int ti = blockIdx.x, g = a.g0, cg = 0, ks = 0;
-    TileInfo cur{};
-    if (ti < ntiles) {
-      g = group_from(a, t_begin + ti, g, lane);
-      cur = tile_at(a, t_begin + ti, g);
-      issue_chunk(cur, 0, 0);
+    // prefetch cursor: kRawBufs - 1 chunks ahead of the one expanded, across
+    // tile boundaries; one commit group per chunk (an empty one past the end)
+    int p_ti = blockIdx.x, p_c = 0, p_g = a.g0, p_buf = 0;
+    TileInfo p_t{};
+    if (p_ti < ntiles) {
+      p_g = group_from(a, t_begin + p_ti, p_g, lane);
+      p_t = tile_at(a, t_begin + p_ti, p_g);
     }
-    float cbf[NV];
-    for (; ti < ntiles && !sm.abort; ti += gridDim.x) {
-      const int tn = ti + gridDim.x;
-      const bool has_next = tn < ntiles;
-      TileInfo nxt{};
-      if (has_next) {
-        g = group_from(a, t_begin + tn, g, lane);
-        nxt = tile_at(a, t_begin + tn, g);
-      }
-      for (int c = 0; c < nchunks; ++c, ++cg) {
-        if (c + 1 < nchunks) {
-          issue_chunk(cur, c + 1, (cg + 1) & 1);
-          cp_async_wait<1>();
-        } else if (has_next) {
-          issue_chunk(nxt, 0, (cg + 1) & 1);
-          cp_async_wait<1>();
-        } else {
-          cp_async_wait<0>();
+    auto prefetch = [&]() {
+      if (p_ti < ntiles) {
+        issue_chunk(p_t, p_c, p_buf);
+        if (++p_c == nchunks) {
+          p_c = 0;
+          p_ti += gridDim.x;
+          if (p_ti < ntiles) {
+            p_g = group_from(a, t_begin + p_ti, p_g, lane);
+            p_t = tile_at(a, t_begin + p_ti, p_g);
+          }
         }
-        const uint8_t* rawr = sm.raw[cg & 1][tid];
+      }
+      cp_async_commit();
+      p_buf = p_buf + 1 == kRawBufs ? 0 : p_buf + 1;
+    };
+    for (int i = 0; i < kRawBufs - 1; ++i) prefetch();
+    float cbf[NV];
+    int cbuf = 0, ks = 0;
+    for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
+      for (int c = 0; c < nchunks; ++c) {
+        prefetch();
+        cp_async_wait<kRawBufs - 1>();  // this chunk's group is complete
+        const uint8_t* rawr = sm.raw[cbuf][tid];
+        cbuf = cbuf + 1 == kRawBufs ? 0 : cbuf + 1;
         if (c == 0) {
 #pragma unroll
           for (int v = 0; v < NV; ++v) cbf[v] = static_cast<float>(reinterpret_cast<const int8_t*>(rawr + SM::CBO)[v]);
         }
-        const int kb = min(kKC, nb - c * kKC);
-        for (int jp = 0; jp < kb / 2; ++jp, ++ks) {
-          const int slot = ks % kStages;
-          if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status)) break;
-          const int jb = 2 * jp + hb;  // block in the chunk
-          float ws;
-          if constexpr (FMT == 4) ws = e8m0_to_f32(rawr[SM::SCL + jb]);
-          else ws = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(rawr + SM::SCL)[jb]);
-          uint32_t cw[4];
-          load_codes<FMT>(rawr + jp * BC, cw);
-          uint32_t tl[4], th[4], ul[4], uh[4];
-          scaled_tables<FMT>(cbf, ws, tl, th, ul, uh);
-          uint32_t vh[16], vl[16];
-          expand_bf16<FMT>(cw, tl, th, vh);
-          if constexpr (NA == 2) expand_bf16<FMT>(cw, ul, uh, vl);
-          tmem_st16(lane_base + a_col<NA>(slot, 0) + 16 * hb, vh);
-          if constexpr (NA == 2) tmem_st16(lane_base + a_col<NA>(slot, 1) + 16 * hb, vl);
+        const int nsc = min(4, nstages - 4 * c);
+        for (int sl = hb; sl < nsc; sl += 2) {
+          const int kg = ks + sl;  // stage in the ring's sequence
+          const int slot = kg % kStages;
+          if (kg >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((kg / kStages) - 1) & 1, a.status)) break;
+          const uint8_t* pair = rawr + 2 * (sl >> 1) * BC;
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+            const int jb = 2 * sl + bb;  // block in the chunk
+            float ws;
+            if constexpr (FMT == 4) ws = e8m0_to_f32(rawr[SM::SCL + jb]);
+            else ws = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(rawr + SM::SCL)[jb]);
+            uint32_t cw[4];
+            load_codes<FMT>(pair + bb * BC, cw);
+            uint32_t tl[4], th[4], ul[4], uh[4];
+            scaled_tables<FMT>(cbf, ws, tl, th, ul, uh);
+            uint32_t vh[16], vl[16];
+            expand_bf16<FMT>(cw, tl, th, vh);
+            if constexpr (NA == 2) expand_bf16<FMT>(cw, ul, uh, vl);
+            tmem_st16(lane_base + a_col<NA>(slot, 0) + 16 * bb, vh);
+            if constexpr (NA == 2) tmem_st16(lane_base + a_col<NA>(slot, 1) + 16 * bb, vl);
+          }
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.full[slot]);
         }
+        ks += nsc;
         if (sm.abort) break;
       }
-      cur = nxt;
     }
     cp_async_wait<0>();
   } else if (warp == kBWarp) {
@@ -705,7 +722,7 @@ int launch_fmt(int fmt, const CUtensorMap& th, const CUtensorMap& tl, const TcAr
 int tc_grouped_gemm(const TcGemm& g, cudaStream_t s) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return MOEQ_ERR_CUDA;
-  if (g.K % 64 || g.R % kTM) return MOEQ_ERR_SHAPE;
+  if (g.K % 128 || g.R % kTM) return MOEQ_ERR_SHAPE;  // an even number of 64-element stages
   CUtensorMap th, tl;
   int rc = act_map(enc, &th, g.act_hi, g.K, g.rows);
   if (!rc) rc = act_map(enc, &tl, g.act_lo, g.K, g.rows);
