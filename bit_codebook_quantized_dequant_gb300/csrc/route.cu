@@ -4,9 +4,9 @@
 // Router ("DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
 // 395", section "Decode: up to 32 tok/s": routing with dedicated TOP_K
 // kernels): a CTA takes 8 tokens; their bf16 rows sit in shared memory and each
-// warp streams router rows from global memory (16-byte loads, lane j reading
-// elements 256 i + 8 j .. +7), accumulating the 8 tokens' dot products in fp32
-// in that order, then the combining rounds 16, 8, 4, 2, 1. The logits stay in
+// warp streams 4 router rows at a time from global memory (16-byte loads, lane j
+// reading elements 256 i + 8 j .. +7), accumulating each of the 8 tokens' dot
+// products in fp32 in that order, then the combining rounds 16, 8, 4, 2, 1. The logits stay in
 // shared memory and one warp per token selects the top k.
 #include <cuda_runtime.h>
 
@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kRtTokens = 8;
 constexpr int kRtWarps = 16;
+constexpr int kRtExp = 4;  // router rows per warp pass
 
 // Top-k + softmax weights of one token by one warp from E logits in memory `l`.
 template <int NPL>
@@ -62,37 +63,50 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_kernel(
     reinterpret_cast<uint4*>(xs + static_cast<size_t>(tt) * H)[c] = v;
   }
   __syncthreads();
-  for (int e = warp; e < E; e += kRtWarps) {
-    const uint16_t* wr = router + static_cast<size_t>(e) * H;
-    float acc[kRtTokens];
+  // a warp takes kRtExp router rows at a time, so that each activation read
+  // from shared memory feeds kRtExp dot products (rows past E read as zero and
+  // are not stored)
+  for (int e0 = warp * kRtExp; e0 < E; e0 += kRtWarps * kRtExp) {
+    float acc[kRtExp][kRtTokens];
 #pragma unroll
-    for (int tt = 0; tt < kRtTokens; ++tt) acc[tt] = 0.0f;
+    for (int j = 0; j < kRtExp; ++j)
+#pragma unroll
+      for (int tt = 0; tt < kRtTokens; ++tt) acc[j][tt] = 0.0f;
     for (int i = 0; i < H / 256; ++i) {
       const int k0 = 256 * i + 8 * lane;
-      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wr + k0));
+      uint4 wv[kRtExp];
+#pragma unroll
+      for (int j = 0; j < kRtExp; ++j)
+        wv[j] = e0 + j < E ? __ldg(reinterpret_cast<const uint4*>(router + static_cast<size_t>(e0 + j) * H + k0))
+                           : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int tt = 0; tt < kRtTokens; ++tt) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xs + static_cast<size_t>(tt) * H + k0);
-        float a = acc[tt];
-        a = fmaf(bf16_lo(xv.x), bf16_lo(wv.x), a);
-        a = fmaf(bf16_hi(xv.x), bf16_hi(wv.x), a);
-        a = fmaf(bf16_lo(xv.y), bf16_lo(wv.y), a);
-        a = fmaf(bf16_hi(xv.y), bf16_hi(wv.y), a);
-        a = fmaf(bf16_lo(xv.z), bf16_lo(wv.z), a);
-        a = fmaf(bf16_hi(xv.z), bf16_hi(wv.z), a);
-        a = fmaf(bf16_lo(xv.w), bf16_lo(wv.w), a);
-        a = fmaf(bf16_hi(xv.w), bf16_hi(wv.w), a);
-        acc[tt] = a;
+#pragma unroll
+        for (int j = 0; j < kRtExp; ++j) {
+          float a = acc[j][tt];
+          a = fmaf(bf16_lo(xv.x), bf16_lo(wv[j].x), a);
+          a = fmaf(bf16_hi(xv.x), bf16_hi(wv[j].x), a);
+          a = fmaf(bf16_lo(xv.y), bf16_lo(wv[j].y), a);
+          a = fmaf(bf16_hi(xv.y), bf16_hi(wv[j].y), a);
+          a = fmaf(bf16_lo(xv.z), bf16_lo(wv[j].z), a);
+          a = fmaf(bf16_hi(xv.z), bf16_hi(wv[j].z), a);
+          a = fmaf(bf16_lo(xv.w), bf16_lo(wv[j].w), a);
+          a = fmaf(bf16_hi(xv.w), bf16_hi(wv[j].w), a);
+          acc[j][tt] = a;
+        }
       }
     }
 #pragma unroll
-    for (int tt = 0; tt < kRtTokens; ++tt) {
-      const float l = warp_sum_canonical(acc[tt]);
-      if (lane == 0) {
-        ls[tt * E + e] = l;
-        if (logits_out && tt < nt) logits_out[static_cast<size_t>(t0 + tt) * E + e] = l;
+    for (int j = 0; j < kRtExp; ++j)
+#pragma unroll
+      for (int tt = 0; tt < kRtTokens; ++tt) {
+        const float l = warp_sum_canonical(acc[j][tt]);
+        if (lane == 0 && e0 + j < E) {
+          ls[tt * E + e0 + j] = l;
+          if (logits_out && tt < nt) logits_out[static_cast<size_t>(t0 + tt) * E + e0 + j] = l;
+        }
       }
-    }
   }
   __syncthreads();
   if (warp < nt)

@@ -108,6 +108,24 @@ def test_route_topk_ties_and_ragged_tail():
         np.testing.assert_array_equal(idx.cpu().numpy().reshape(T, k)[t], O.topk(ref[t], k)[0])
 
 
+def test_route_topk_expert_count_not_multiple_of_4():
+    # the kernel takes router rows four at a time; E = 37 leaves a partial group
+    H, E, k, T = 512, 37, 3, 9
+    rng = np.random.default_rng(6)
+    x = S.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wr = S.f32_to_bf16_bits((rng.standard_normal((E, H)) * 0.05).astype(np.float32))
+    idx = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    w = torch.zeros(T * k, dtype=torch.float32, device="cuda")
+    lg = torch.full((T * E + 8,), 7.0, dtype=torch.float32, device="cuda")
+    M.moe_route_topk(to_dev_u16(x), T, to_dev_u16(wr), E, H, k, idx, w, lg)
+    ref = O.router_logits(x, wr)
+    out = lg.cpu().numpy()
+    np.testing.assert_array_equal(out[:T * E].reshape(T, E), ref)
+    assert np.all(out[T * E:] == 7.0)  # nothing written past T x E
+    for t in range(T):
+        np.testing.assert_array_equal(idx.cpu().numpy().reshape(T, k)[t], O.topk(ref[t], k)[0])
+
+
 def test_rmsnorm_bit_exact():
     rng = np.random.default_rng(5)
     T, H = 19, 4096
