@@ -40,8 +40,11 @@
 //   10-17 epilogue, two warps per TMEM lane quarter (64 columns each), once
 //         per tile
 // Rings (mbarriers, every wait bounded): 4 operand stages (B in shared memory,
-// A in TMEM), 2 TMEM tile accumulators (the epilogue of one tile overlaps the
-// next tile's main loop).
+// A in TMEM; a stage is full when both its barriers are: the producer's copies
+// and the 4 expansion warps' stores), 2 TMEM tile accumulators (the epilogue
+// of one tile overlaps the next tile's main loop). Before the CTA exits, the
+// producer waits for the copies of its last stages, the MMA issuer for all of
+// its MMAs and the expansion threads for their cp.async groups.
 //
 // Sources: "DeepSeek V4 Flash: 284B model, up to 32 tok/s on AMD Ryzen AI MAX+
 // 395", section "ROCmFPX: fitting 284B weights into 128 GB" (small codebooks
@@ -87,7 +90,9 @@ struct TcSmem {
   static constexpr int CBO = SCL + 16;
   uint8_t b[kStages][2][kTN * 128];   // activation parts: 128 rows x 64 bf16, SW128 K-major
   uint8_t raw[kRawBufs][kExpWarps * 32][RPT];
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full_a[kStages];            // weight stage in TMEM: the 4 expansion warps of its parity
+  uint64_t full_b[kStages];            // activation stage in shared memory: the producer + its bytes
+  uint64_t empty[kStages];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;                     // completion of every MMA this CTA issued
   uint32_t nmma[kStages];             // MMA N of the stage (its tile's rows, rounded up to 16)
@@ -378,7 +383,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm.full[i], 5);  // the 4 expansion warps of the stage's parity + the activation producer (+ its bytes)
+      mbar_init(&sm.full_a[i], 4);
+      mbar_init(&sm.full_b[i], 1);
       mbar_init(&sm.empty[i], 1);             // MMA commit
     }
     for (int i = 0; i < kAccBufs; ++i) {
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.full[slot]);
+          if (lane == 0) mbar_arrive(&sm.full_a[slot]);
         }
         ks += nsc;
         if (sm.abort) break;
@@ -520,7 +526,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     cp_async_wait<0>();
   } else if (warp == kBWarp) {
     // ------------------------------------------------------------ activation producer
-    int ks = 0, g = a.g0;
+    int ks = 0, g = a.g0;  // ks: stages issued
     for (int ti = blockIdx.x; ti < ntiles && !sm.abort; ti += gridDim.x) {
       g = group_from(a, t_begin + ti, g, lane);
       const TileInfo t = tile_at(a, t_begin + ti, g);
@@ -533,15 +539,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         if (ks >= kStages && !warp_wait<FMT>(sm, &sm.empty[slot], ((ks / kStages) - 1) & 1, a.status)) break;
         if (lane == 0) {
           sm.nmma[slot] = nm;
-          mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(2 * nbox * kBoxRows * 128));
+          mbar_arrive_expect_tx(&sm.full_b[slot], static_cast<uint32_t>(2 * nbox * kBoxRows * 128));
           for (int bx = 0; bx < nbox; ++bx) {
-            tma_load_2d(sm.b[slot][0] + bx * kBoxRows * 128, &tm_hi, 64 * p, y0 + bx * kBoxRows, &sm.full[slot]);
-            tma_load_2d(sm.b[slot][1] + bx * kBoxRows * 128, &tm_lo, 64 * p, y0 + bx * kBoxRows, &sm.full[slot]);
+            tma_load_2d(sm.b[slot][0] + bx * kBoxRows * 128, &tm_hi, 64 * p, y0 + bx * kBoxRows, &sm.full_b[slot]);
+            tma_load_2d(sm.b[slot][1] + bx * kBoxRows * 128, &tm_lo, 64 * p, y0 + bx * kBoxRows, &sm.full_b[slot]);
           }
         }
         __syncwarp();
       }
     }
+    // the copies of the last use of each slot have landed before the CTA may
+    // exit (they have, unless a wait ran out and the MMA stopped consuming)
+    if (lane == 0) {
+      for (int j = max(0, ks - kStages); j < ks; ++j) {
+        bool done = false;
+        for (uint32_t i = 0; i < kSpinLimit && !done; ++i)
+          done = mbar_try_wait_sleep(&sm.full_b[j % kStages], (j / kStages) & 1);
+        if (!done) {
+          set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
@@ -558,7 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         const uint32_t dcol = tmem + static_cast<uint32_t>(tb * kTN);
         for (int p = 0; p < nstages && ok; ++p, ++ks) {
           const int slot = ks % kStages;
-          if (!(ok = ring_wait<FMT>(sm, &sm.full[slot], (ks / kStages) & 1, a.status))) break;
+          if (!(ok = ring_wait<FMT>(sm, &sm.full_b[slot], (ks / kStages) & 1, a.status))) break;
+          if (!(ok = ring_wait<FMT>(sm, &sm.full_a[slot], (ks / kStages) & 1, a.status))) break;
           tc_fence_after();
           const uint32_t idesc = kIdescM | ((sm.nmma[slot] >> 3) << 17);
 #pragma unroll
