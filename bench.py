@@ -331,7 +331,7 @@ def bench_prefill(args, cid, T, tc_peak, hbm_peak, peak_kind):
                         "traffic_scope": "DRAM bytes of the gate, up and down tensor-core "
                                          "launches of one call (routed experts)",
                         "peak_source": f"{peak_kind} bf16_tflops (the prefill contraction runs "
-                                       "bf16-exact integer products)",
+                                       "as bf16 part products on the tensor cores)",
                         "algorithmic_flops_per_launch": fl,
                         "hbm_frac_weights": wbytes / (ms * 1e-3) / 1e9 / hbm_peak},
            "gpu_launches_per_call": prefill_launches(cfg)}
