@@ -32,7 +32,11 @@ import numpy as np  # noqa: E402
 
 WORKLOAD = ("decode-b1: H=4096 I=2048 E=256 top-6 + shared expert; routed gate/up FP2 (10 B/32), "
             "routed down FP3 (14 B/32), shared FP4 (17 B/32), bf16 router")
-CFG_ID = 1
+DECODE_WORKLOAD = "decode-b1"
+# the headline line's value is decode b=1 (one layer); the q=4 verification and
+# the 32K prefill are reported beside it ("verify_q4", "prefill"), each with its
+# roofline fraction
+DECODE_METRIC = "MoE-FFN tok/s (decode b=1, q=4 verify, 32K prefill) + % of HBM/TC roofline"
 
 
 def algorithmic_bytes_decode(cfg: dict) -> int:
@@ -178,14 +182,14 @@ def _dist():
     return ws, rank, local
 
 
-def cpu_baseline(cfg_id: int, tokens: int, seconds_cap: float = 30.0):
+def cpu_baseline(name: str, tokens: int, seconds_cap: float = 30.0):
     """The oracle, as it stands, timed on this host (one core) on a bounded
     sample of the workload's tokens. Returns (tokens/s, sample description)."""
     import oracle as O
     from oracle import workload as W
     from bit_codebook_quantized_dequant_gb300 import synth as S
-    cfg = S.CONFIGS[cfg_id]
-    seed = S.config_seed(cfg_id)
+    cfg = S.WORKLOADS[name]
+    seed = S.workload_seed(name)
     xs = S.tokens(seed, cfg, tokens)
     experts = set()
     wr = S.router_weights(seed, 0, cfg)
@@ -208,8 +212,8 @@ def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return
-    tps, sample, dt = cpu_baseline(CFG_ID, max(1, min(args.steps, 4)))
-    line = {"impl": "reference", "metric": "MoE-FFN decode tok/s", "value": tps,
+    tps, sample, dt = cpu_baseline(DECODE_WORKLOAD, max(1, min(args.steps, 4)))
+    line = {"impl": "reference", "metric": DECODE_METRIC, "value": tps,
             "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 / tps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -242,9 +246,9 @@ def bench_verify(args, hbm_peak, peak_kind):
     import bit_codebook_quantized_dequant_gb300 as M
     from bit_codebook_quantized_dequant_gb300 import synth as S
     from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, to_dev_u16
-    cid = 2
-    cfg = S.CONFIGS[cid]
-    seed = S.config_seed(cid)
+    name = "verify-q4"
+    cfg = S.WORKLOADS[name]
+    seed = S.workload_seed(name)
     R = 2
     layers = [build_layer(seed, r, cfg) for r in range(R)]
     wss = [Workspace(dl, 1) for dl in layers]
@@ -296,14 +300,14 @@ def bench_verify(args, hbm_peak, peak_kind):
     return out
 
 
-def bench_prefill(args, cid, T, tc_peak, hbm_peak, peak_kind):
+def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind):
     """Expert-grouped prefill of T tokens through one layer (moe_ffn_prefill)."""
     import torch
     import bit_codebook_quantized_dequant_gb300 as M
     from bit_codebook_quantized_dequant_gb300 import synth as S
     from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, to_dev_u16
-    cfg = S.CONFIGS[cid]
-    seed = S.config_seed(cid)
+    cfg = S.WORKLOADS[name]
+    seed = S.workload_seed(name)
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 2, T)
     X = to_dev_u16(S.tokens(seed, cfg, T))
@@ -323,10 +327,10 @@ def bench_prefill(args, cid, T, tc_peak, hbm_peak, peak_kind):
     wbytes = dl.weight_bytes()
     out = {"metric": "prefill tok/s (one layer)", "value": T / (ms * 1e-3), "unit": "tok/s",
            "ms_per_call": ms, "calls": steps, "tokens": T,
-           "workload": S.CONFIGS[cid]["name"] + f": T={T}, all 256 experts' weights read once",
+           "workload": name + f": T={T}, all 256 experts' weights read once",
            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
                         "frac": tflops / tc_peak,
-                        "traffic": _traffic(f"prefill cfg{cid} gemm",
+                        "traffic": _traffic(f"prefill {name} gemm",
                                             "bit_codebook_quantized_dequant_gb300/csrc/gemm_tc.cu"),
                         "traffic_scope": "DRAM bytes of the gate, up and down tensor-core "
                                          "launches of one call (routed experts)",
@@ -348,9 +352,9 @@ def run_sections(args, hbm_peak, tc_peak, peak_kind):
         out["verify_q4"] = bench_verify(args, hbm_peak, peak_kind)
     pre = []
     if "prefill" in sec or "prefill3" in sec:
-        pre.append(bench_prefill(args, 3, args.prefill_tokens or 2048, tc_peak, hbm_peak, peak_kind))
+        pre.append(bench_prefill(args, "prefill-h32-fp4", args.prefill_tokens or 2048, tc_peak, hbm_peak, peak_kind))
     if "prefill" in sec or "prefill4" in sec:
-        pre.append(bench_prefill(args, 4, args.prefill_tokens or 32512, tc_peak, hbm_peak, peak_kind))
+        pre.append(bench_prefill(args, "prefill-43-layer-stack", args.prefill_tokens or 32512, tc_peak, hbm_peak, peak_kind))
     if pre:
         out["prefill"] = pre
     return out
@@ -374,8 +378,8 @@ def run(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    cfg = S.CONFIGS[CFG_ID]
-    seed = S.config_seed(CFG_ID)
+    cfg = S.WORKLOADS[DECODE_WORKLOAD]
+    seed = S.workload_seed(DECODE_WORKLOAD)
     M.load()
     R = args.replicas
     layers = [build_layer(seed, r, cfg) for r in range(R)]
@@ -451,7 +455,7 @@ def run(args):
     e2e = job_throughput(world, args.steps, ms_e2e)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        tps, sample, _ = cpu_baseline(CFG_ID, 20)
+        tps, sample, _ = cpu_baseline(DECODE_WORKLOAD, 20)
         cpu = {"value": tps, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample}
     traffic = _traffic("ffn_kernel<1>", "bit_codebook_quantized_dequant_gb300/csrc/decode.cu")
     wbytes = R * layers[0].weight_bytes()
@@ -461,7 +465,7 @@ def run(args):
         torch.cuda.empty_cache()
         extra = run_sections(args, hbm_peak, tc_peak, peak_kind)
     line = {
-        "metric": "MoE-FFN decode tok/s (batch 1, one layer)",
+        "metric": DECODE_METRIC,
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8-dot/fp32",

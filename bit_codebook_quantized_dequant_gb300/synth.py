@@ -68,8 +68,9 @@ KIND_CODEBOOK = 2
 KIND_VALUES = 3
 
 
-def config_seed(config_id: int) -> int:
-    return 0xC0FFEE00 + int(config_id)
+def workload_seed(name: str) -> int:
+    """Base seed of a workload preset (position of its name in WORKLOAD_ORDER)."""
+    return 0xC0FFEE00 + WORKLOAD_ORDER.index(name)
 
 
 def stream_id(layer: int, role: int, expert: int = 0, kind: int = 0) -> int:
@@ -186,18 +187,19 @@ def signs(seed: int, stream: int, n: int) -> np.ndarray:
 # Workload presets. Shapes and formats of the five seeded workloads; values are
 # drawn with the generators above, stream ids from ``stream_id``.
 # ---------------------------------------------------------------------------
-CONFIGS = {
-    0: dict(name="tiny-decode", H=256, I=128, E=16, k=2, fmt_gu=2, fmt_down=3, shared_fmt=None,
+WORKLOADS = {
+    "tiny-decode": dict(name="tiny-decode", H=256, I=128, E=16, k=2, fmt_gu=2, fmt_down=3, shared_fmt=None,
             h32=False, T=1, layers=1, dense=False),
-    1: dict(name="decode-b1", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3, shared_fmt=4,
+    "decode-b1": dict(name="decode-b1", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3, shared_fmt=4,
             h32=False, T=1, layers=1, dense=False),
-    2: dict(name="verify-q4", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3, shared_fmt=4,
+    "verify-q4": dict(name="verify-q4", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3, shared_fmt=4,
             h32=False, T=4, layers=1, dense=True),
-    3: dict(name="prefill-h32-fp4", H=4096, I=2048, E=256, k=6, fmt_gu=4, fmt_down=4,
+    "prefill-h32-fp4": dict(name="prefill-h32-fp4", H=4096, I=2048, E=256, k=6, fmt_gu=4, fmt_down=4,
             shared_fmt=None, h32=True, T=2048, layers=1, dense=False),
-    4: dict(name="prefill-43-layer-stack", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3,
+    "prefill-43-layer-stack": dict(name="prefill-43-layer-stack", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3,
             shared_fmt=4, h32=False, T=32512, layers=43, dense=False),
 }
+WORKLOAD_ORDER = ("tiny-decode", "decode-b1", "verify-q4", "prefill-h32-fp4", "prefill-43-layer-stack")
 
 # (role, rows-is-I?) for the matrices of a layer: gate/up are [I x H], down [H x I]
 MATRIX_ROLES = {

@@ -29,7 +29,7 @@ def _rank_main(rank, world, port, out):
     times = [10.0 + 5.0 * rank, 20.0 - 3.0 * rank]  # this rank's timed regions (ms)
     ms, ms_e2e = bench.max_over_ranks(times, dist)
     start = bench.rank_token_start(r, 8)
-    x = S.tokens(S.config_seed(0), S.CONFIGS[0], 8, start=start)
+    x = S.tokens(S.workload_seed("tiny-decode"), S.WORKLOADS["tiny-decode"], 8, start=start)
     out[rank] = (ws, r, local, ms, ms_e2e, start, x.tobytes())
     dist.barrier()
     dist.destroy_process_group()
@@ -49,7 +49,7 @@ def test_two_gloo_ranks_weak_scaling():
     # disjoint token streams: rank 1's tokens are the continuation of rank 0's
     x0 = np.frombuffer(res[0][6], dtype=np.uint16)
     x1 = np.frombuffer(res[1][6], dtype=np.uint16)
-    both = S.tokens(S.config_seed(0), S.CONFIGS[0], 16).ravel()
+    both = S.tokens(S.workload_seed("tiny-decode"), S.WORKLOADS["tiny-decode"], 16).ravel()
     np.testing.assert_array_equal(np.concatenate([x0, x1]), both)
     # whole-job throughput: all ranks' units over the slowest rank's time
     assert bench.job_throughput(world, 1000, 15.0) == pytest.approx(2 * 1000 / 0.015)

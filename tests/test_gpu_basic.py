@@ -18,7 +18,7 @@ def _status():
 
 @pytest.mark.parametrize("bits", [2, 3, 4])
 def test_generator_twin_matches_host(bits):
-    seed, stream = S.config_seed(1), S.stream_id(3, S.ROLE_GATE, 77, S.KIND_CODES)
+    seed, stream = S.workload_seed("decode-b1"), S.stream_id(3, S.ROLE_GATE, 77, S.KIND_CODES)
     rows, cols = 37, 256
     out = torch.empty(rows * cols, dtype=torch.uint8, device="cuda")
     M.moeq_synth_codes(seed, stream, bits, rows * cols, out)
@@ -73,10 +73,10 @@ def test_h32_rotate_bit_exact():
     np.testing.assert_array_equal(d_in.cpu().numpy(), O.h32_f32(v, None))
 
 
-@pytest.mark.parametrize("cfg_id,T", [(0, 13), (1, 37)])
-def test_route_topk_bit_exact(cfg_id, T):
-    cfg = S.CONFIGS[cfg_id]
-    seed = S.config_seed(cfg_id)
+@pytest.mark.parametrize("name,T", [("tiny-decode", 13), ("decode-b1", 37)])
+def test_route_topk_bit_exact(name, T):
+    cfg = S.WORKLOADS[name]
+    seed = S.workload_seed(name)
     wr = S.router_weights(seed, 0, cfg)
     x = S.tokens(seed, cfg, T)
     E, H, k = cfg["E"], cfg["H"], cfg["k"]

@@ -16,8 +16,8 @@ from _parity import check_output, check_token, host_layer_for
 pytestmark = pytest.mark.gpu
 
 
-def _cfg(cfg_id, **over):
-    c = dict(S.CONFIGS[cfg_id])
+def _cfg(name, **over):
+    c = dict(S.WORKLOADS[name])
     c.update(over)
     return c
 
@@ -42,8 +42,8 @@ def test_decode_tiny(variant):
         over = dict(h32=True, fmt_gu=4, fmt_down=4)
     elif variant == "cfg0-fp2-down":
         over = dict(fmt_down=2, shared_fmt=4)
-    cfg = _cfg(0, **over)
-    seed = S.config_seed(0) + 17 * len(variant)
+    cfg = _cfg("tiny-decode", **over)
+    seed = S.workload_seed("tiny-decode") + 17 * len(variant)
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 0)
     xs = S.tokens(seed, cfg, 8)
@@ -56,8 +56,8 @@ def test_decode_tiny(variant):
 
 
 def test_decode_config1_sampled_tokens():
-    cfg = _cfg(1)
-    seed = S.config_seed(1)
+    cfg = _cfg("decode-b1")
+    seed = S.workload_seed("decode-b1")
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 0)
     xs = S.tokens(seed, cfg, 3, start=0)
@@ -68,8 +68,8 @@ def test_decode_config1_sampled_tokens():
 
 
 def test_decode_repeatable_and_workspace_reused():
-    cfg = _cfg(1)
-    seed = S.config_seed(1)
+    cfg = _cfg("decode-b1")
+    seed = S.workload_seed("decode-b1")
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 0)
     xs = S.tokens(seed, cfg, 2, start=100)

@@ -18,8 +18,8 @@ from _parity import FLIPS_PREFILL, PREFILL, check_output, check_token, column_vi
 pytestmark = pytest.mark.gpu
 
 
-def _cfg(cfg_id, **over):
-    c = dict(S.CONFIGS[cfg_id])
+def _cfg(name, **over):
+    c = dict(S.WORKLOADS[name])
     c.update(over)
     return c
 
@@ -53,8 +53,8 @@ def test_prefill_tiny(variant):
         over = dict(shared_fmt=4, k=3)
     elif variant == "cfg0-h32-fp4":
         over = dict(h32=True, fmt_gu=4, fmt_down=4)
-    cfg = _cfg(0, **over)
-    seed = S.config_seed(0) + 31 * len(variant)
+    cfg = _cfg("tiny-decode", **over)
+    seed = S.workload_seed("tiny-decode") + 31 * len(variant)
     dl = build_layer(seed, 0, cfg)
     T = 300  # several 64-row tiles per expert group and a ragged last one
     X = S.tokens(seed, cfg, T)
@@ -63,8 +63,8 @@ def test_prefill_tiny(variant):
 
 
 def test_prefill_config3_sampled_tokens():
-    cfg = _cfg(3)
-    seed = S.config_seed(3)
+    cfg = _cfg("prefill-h32-fp4")
+    seed = S.workload_seed("prefill-h32-fp4")
     dl = build_layer(seed, 0, cfg)
     T = 256
     X = S.tokens(seed, cfg, T)
@@ -72,8 +72,8 @@ def test_prefill_config3_sampled_tokens():
 
 
 def test_prefill_matches_decode_and_residual():
-    cfg = _cfg(1)
-    seed = S.config_seed(1)
+    cfg = _cfg("decode-b1")
+    seed = S.workload_seed("decode-b1")
     dl = build_layer(seed, 0, cfg)
     T = 70
     X = S.tokens(seed, cfg, T, start=500)
@@ -106,8 +106,8 @@ def test_prefill_matches_decode_and_residual():
 
 
 def test_prefill_edge_cases():
-    cfg = _cfg(0)
-    seed = S.config_seed(0) + 3
+    cfg = _cfg("tiny-decode")
+    seed = S.workload_seed("tiny-decode") + 3
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 2, 8)
     y = torch.zeros(8 * cfg["H"], dtype=torch.float32, device="cuda")

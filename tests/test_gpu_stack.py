@@ -29,8 +29,8 @@ SAMPLE = [0, 41, 63]
 
 
 def test_stack_matches_composition_and_oracle():
-    cfg = dict(S.CONFIGS[4])
-    seed = S.config_seed(4)
+    cfg = dict(S.WORKLOADS["prefill-43-layer-stack"])
+    seed = S.workload_seed("prefill-43-layer-stack")
     layers = [build_layer(seed, l, cfg) for l in range(NL)]
     H = cfg["H"]
     X = S.tokens(seed, cfg, T)

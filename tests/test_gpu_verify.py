@@ -19,8 +19,8 @@ from _parity import check_output, check_token, column_view, host_layer_for
 pytestmark = pytest.mark.gpu
 
 
-def _cfg(cfg_id, **over):
-    c = dict(S.CONFIGS[cfg_id])
+def _cfg(name, **over):
+    c = dict(S.WORKLOADS[name])
     c.update(over)
     return c
 
@@ -84,8 +84,8 @@ def test_verify_tiny(variant, pattern):
         over.update(shared_fmt=4, k=3)
     else:
         over.update(h32=True, fmt_gu=4, fmt_down=4)
-    cfg = _cfg(0, **over)
-    seed = S.config_seed(0) + 101 * len(variant)
+    cfg = _cfg("tiny-decode", **over)
+    seed = S.workload_seed("tiny-decode") + 101 * len(variant)
     dl = build_layer(seed, 0, cfg)
     ws, ws1 = Workspace(dl, 1), Workspace(dl, 0)
     xs = S.tokens(seed, cfg, 12)
@@ -99,8 +99,8 @@ def test_verify_tiny(variant, pattern):
 
 
 def test_verify_config2_sampled_batches():
-    cfg = _cfg(2)
-    seed = S.config_seed(2)
+    cfg = _cfg("verify-q4")
+    seed = S.workload_seed("verify-q4")
     dl = build_layer(seed, 0, cfg)
     ws, ws1 = Workspace(dl, 1), Workspace(dl, 0)
     xs = S.tokens(seed, cfg, 8)
@@ -110,8 +110,8 @@ def test_verify_config2_sampled_batches():
 
 
 def test_verify_without_dense_and_repeatable():
-    cfg = _cfg(2)
-    seed = S.config_seed(2)
+    cfg = _cfg("verify-q4")
+    seed = S.workload_seed("verify-q4")
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 1)
     X = S.tokens(seed, cfg, 4, start=40)

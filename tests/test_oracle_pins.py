@@ -107,8 +107,8 @@ def test_generator_distributions():
     assert abs(x.mean()) < 0.01 and abs(x.std() - 1.0) < 0.01
     # rows drawn alone equal the same rows drawn with the whole matrix
     np.testing.assert_array_equal(S.codes_rows(3, 12, 3, 256, 10, 5), c[10:15])
-    np.testing.assert_array_equal(S.tokens(3, S.CONFIGS[0], 3, start=4),
-                                  S.tokens(3, S.CONFIGS[0], 8)[4:7])
+    np.testing.assert_array_equal(S.tokens(3, S.WORKLOADS["tiny-decode"], 3, start=4),
+                                  S.tokens(3, S.WORKLOADS["tiny-decode"], 8)[4:7])
 
 
 # ----------------------------------------------------------------- Q8
@@ -208,8 +208,8 @@ def test_router_order_golden():
 
 
 def test_router_within_fp32_bound_of_fp64():
-    cfg = S.CONFIGS[1]
-    seed = S.config_seed(1)
+    cfg = S.WORKLOADS["decode-b1"]
+    seed = S.workload_seed("decode-b1")
     wr = S.router_weights(seed, 0, cfg)[:32]
     x = S.tokens(seed, cfg, 2)
     lg = O.router_logits(x, wr)
@@ -251,7 +251,7 @@ def _dense(m: O.Matrix, e: int, codes: np.ndarray) -> np.ndarray:
 
 @pytest.mark.parametrize("name", ["gate", "down", "sgate"])
 def test_matvec_equals_dense_brute_force(name):
-    cfg = dict(S.CONFIGS[1])
+    cfg = dict(S.WORKLOADS["decode-b1"])
     cfg.update(H=256, I=128)
     seed = 11
     m = W.matrix(seed, 0, cfg, name, [3] if name != "sgate" else [0])
@@ -304,7 +304,7 @@ def _brute_ffn(cfg, seed, L, x, idx_p):
 
 @pytest.mark.parametrize("variant", ["tiny", "tiny-shared", "tiny-h32"])
 def test_ffn_decode_equals_brute_force(variant):
-    cfg = dict(S.CONFIGS[0])
+    cfg = dict(S.WORKLOADS["tiny-decode"])
     if variant == "tiny-shared":
         cfg.update(shared_fmt=4, k=3)
     if variant == "tiny-h32":
@@ -325,7 +325,7 @@ def test_ffn_decode_equals_brute_force(variant):
 
 
 def test_expert_relabelling_invariance():
-    cfg = S.CONFIGS[0]
+    cfg = S.WORKLOADS["tiny-decode"]
     seed = 22
     L = W.layer(seed, 0, cfg, range(cfg["E"]))
     x = S.tokens(seed, cfg, 2)
@@ -344,7 +344,7 @@ def test_expert_relabelling_invariance():
 
 
 def test_teacher_forcing_replaces_quantized_h():
-    cfg = S.CONFIGS[0]
+    cfg = S.WORKLOADS["tiny-decode"]
     seed = 23
     L = W.layer(seed, 0, cfg, range(cfg["E"]))
     x = S.tokens(seed, cfg, 1)[0]
@@ -358,7 +358,7 @@ def test_teacher_forcing_replaces_quantized_h():
 
 
 def test_prefill_and_q4_are_per_token_decode():
-    cfg = dict(S.CONFIGS[0])
+    cfg = dict(S.WORKLOADS["tiny-decode"])
     cfg.update(dense=True, shared_fmt=4)
     seed = 24
     L = W.layer(seed, 0, cfg, range(cfg["E"]))

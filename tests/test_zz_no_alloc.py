@@ -15,10 +15,10 @@ from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cfg_id", [0, 1])
-def test_static_scratch_matches_workspace_decode(cfg_id):
-    cfg = dict(S.CONFIGS[cfg_id])
-    seed = S.config_seed(cfg_id) + 7
+@pytest.mark.parametrize("name", ["tiny-decode", "decode-b1"])
+def test_static_scratch_matches_workspace_decode(name):
+    cfg = dict(S.WORKLOADS[name])
+    seed = S.workload_seed(name) + 7
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 0)
     xs = S.tokens(seed, cfg, 2, start=300)
