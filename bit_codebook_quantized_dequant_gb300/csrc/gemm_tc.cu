@@ -3,13 +3,15 @@
 // One tile = 128 weight rows x up to 128 grouped rows (tokens of one expert),
 // the whole contraction K. The block scales are folded into the operands and
 // the operands split into bf16 parts:
-//   weights  a = cb[code] * ws[r, b]   (<= 19 significant bits, exact in fp32)
+//   weights  a = cb[code] * ws[r, b]   (<= 18 significant bits, exact in fp32)
 //   activ.   x = q * d[t, b]            (<= 18 significant bits, exact in fp32)
 //   a = a_hi + a_lo, x = x_hi + x_lo with a_hi = bf16(a), a_lo = bf16(a - a_hi)
-//   (what the two parts leave out is below 2^-18 of the value; for power-of-two
-//   (E8M0) weight scales a is a bf16 value itself and a_lo = 0)
-// and a . x = a_hi x_hi + a_hi x_lo + a_lo x_hi, each product exact in the fp32
-// accumulator; the term left out, a_lo x_lo, is below 2^-18 of |a x|.
+//   (|lo| < 2^-8 |v|; what the two parts leave out is below 2^-17 of the value
+//   over every int8 code and fp16 scale; for power-of-two (E8M0) weight scales
+//   a is a bf16 value itself and a_lo = 0)
+// and a . x ~ a_hi x_hi + a_hi x_lo + a_lo x_hi, each product exact in the fp32
+// accumulator; with the term left out, a_lo x_lo (below 2^-16 of |a x|), the
+// kept products differ from a x by less than 8 * 2^-18 (3.1e-5) of |a x|.
 // tcgen05.mma kind::f16 accumulates the products and all 32-element blocks of
 // K into one TMEM accumulator per tile, read out once per tile -- no per-block
 // hand-off between the tensor cores and the CUDA cores. The only difference to
@@ -254,7 +256,7 @@ __device__ __forceinline__ void scaled_tables(const float* cbf, float ws, uint32
   for (int w = 0; w < NV / 4; ++w) {
     float t[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) t[j] = __fmul_rn(cbf[4 * w + j], ws);  // exact: <= 19 significant bits
+    for (int j = 0; j < 4; ++j) t[j] = __fmul_rn(cbf[4 * w + j], ws);  // exact: <= 18 significant bits
     uint32_t hp[2], lp[2];
     split4(t, hp, lp);
     planes(hp[0], hp[1], tl[w], th[w]);
