@@ -66,9 +66,10 @@ def check_output(y_gpu, y_ref, bound, what=""):
 # quantization and the fp64 oracle's own (each side quantizes its own h; the
 # GPU's h is checked against the oracle's quantizer bit for bit regardless).
 # Decode and q=4 sum exact int32 block partials in fp32: 0.1 %. The prefill's
-# tensor-core operands carry code x scale to 16 significant bits (the part
-# below 2^-16 of each value is left out), so h differs from the oracle's by
-# up to ~3e-5 relative and ~0.2 % of the codes flip (measured): 1 %.
+# tensor-core operands carry code x scale in two bf16 parts (what they leave
+# out, with the low x low product, is below 8 * 2^-18 of |w x| per product,
+# tests/test_prefill_split_bound.py), so its h differs from the oracle's by a
+# few 1e-5 relative and 0.1-0.2 % of the codes flip (measured): 1 %.
 FLIPS_DECODE = 1e-3
 FLIPS_PREFILL = 1e-2
 # Absolute tolerance of h, as a fraction of the token's max |h|: the prefill's
