@@ -1,5 +1,6 @@
 // Expert-grouped prefill of T tokens: every token gets the decode's result
-// (up to fp32 summation order), computed as
+// up to the rounding of the tensor-core contraction (bf16 operand parts, fp32
+// sums; gemm_tc.cu), computed as
 //   router + top-k of every token              (route.cu)
 //   Q8 of every 32-block of x (after H32)       prep_x_kernel
 //   stable counting sort of the (token, slot) pairs by expert

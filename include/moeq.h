@@ -222,10 +222,15 @@ int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, const uint1
 
 /* Expert-grouped prefill of T tokens ("deepseek-v4-flash-0731-evox3-rocm",
  * section "The optimization ladder": fused multi-token prefill): per token
- * the same result as moe_ffn_decode up to fp32 summation order, computed as
- * router + top-k for all tokens, a stable counting sort of the (token, slot)
- * pairs by expert (ascending token, then slot), grouped GEMMs for gate/up
- * (+SwiGLU, H32, Q8 of h) and down, and a gather-combine in slot order. If
+ * the result of moe_ffn_decode (bit-identical xq, xd, logits, indices and
+ * weights) up to the rounding of the tensor-core contraction: the weights
+ * (code x block scale) and activations (code x scale) enter as two bf16
+ * parts each, and the products a_hi x_hi + a_hi x_lo + a_lo x_hi are within
+ * 3.1e-5 of each a x, summed in fp32. Computed as router + top-k for all
+ * tokens, a stable counting sort of the (token, slot) pairs by expert
+ * (ascending token, then slot), grouped GEMMs for gate/up (+SwiGLU, H32, Q8
+ * of h) and down on the tensor cores, and a gather-combine in slot order.
+ * H and I must be multiples of 128 (as every matrix's cols). If
  * residual is not NULL, y = residual + FFN(x) rounded once (the residual add
  * of a stacked layer; y may equal residual). x [T x H] bf16, y [T x H] fp32.
  * ws: at least moe_ffn_workspace(L, T, 2) bytes (contents need no zeroing);
