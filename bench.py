@@ -208,6 +208,27 @@ def cpu_baseline(name: str, tokens: int, seconds_cap: float = 30.0):
     return done / dt, f"{done} tokens of the decode workload (layer 0), oracle single-threaded", dt
 
 
+def cpu_baseline_prefill(name: str, tokens: int = 8) -> dict:
+    """The oracle's prefill, as it stands, timed on this host (one core) on the
+    first `tokens` tokens of a prefill workload (one layer). Each token's FFN
+    is independent of the others, so the rate holds for all T tokens."""
+    import oracle as O
+    from oracle import workload as W
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    cfg = S.WORKLOADS[name]
+    seed = S.workload_seed(name)
+    xs = S.tokens(seed, cfg, tokens)
+    idx, _ = W.route(seed, 0, cfg, xs)
+    L = W.layer(seed, 0, cfg, {int(e) for r in idx for e in r})
+    t0 = time.perf_counter()
+    O.ffn_prefill(L, xs)
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"the first {tokens} tokens of the {name} workload (layer 0) through the "
+                      "oracle's prefill, single-threaded; each token's FFN is independent of "
+                      "the others, so the rate holds for all T tokens"}
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -300,7 +321,7 @@ def bench_verify(args, hbm_peak, peak_kind):
     return out
 
 
-def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind):
+def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind, cpu=False):
     """Expert-grouped prefill of T tokens through one layer (moe_ffn_prefill)."""
     import torch
     import bit_codebook_quantized_dequant_gb300 as M
@@ -341,20 +362,28 @@ def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind):
            "gpu_launches_per_call": prefill_launches(cfg)}
     del dl, ws
     torch.cuda.empty_cache()
+    if cpu:
+        try:
+            out["cpu_baseline"] = cpu_baseline_prefill(name)
+        except Exception as e:  # the GPU numbers stand without it
+            out["cpu_baseline"] = {"error": repr(e)}
     return out
 
 
-def run_sections(args, hbm_peak, tc_peak, peak_kind):
-    """The q=4 verification and prefill sections named in --sections."""
+def run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=False):
+    """The q=4 verification and prefill sections named in --sections (cpu: add
+    the oracle's prefill rate on the host to each prefill section)."""
     sec = args.sections.split(",")
     out = {}
     if "verify" in sec:
         out["verify_q4"] = bench_verify(args, hbm_peak, peak_kind)
     pre = []
     if "prefill" in sec or "prefill3" in sec:
-        pre.append(bench_prefill(args, "prefill-h32-fp4", args.prefill_tokens or 2048, tc_peak, hbm_peak, peak_kind))
+        pre.append(bench_prefill(args, "prefill-h32-fp4", args.prefill_tokens or 2048, tc_peak, hbm_peak,
+                                 peak_kind, cpu))
     if "prefill" in sec or "prefill4" in sec:
-        pre.append(bench_prefill(args, "prefill-43-layer-stack", args.prefill_tokens or 32512, tc_peak, hbm_peak, peak_kind))
+        pre.append(bench_prefill(args, "prefill-43-layer-stack", args.prefill_tokens or 32512, tc_peak,
+                                 hbm_peak, peak_kind, cpu))
     if pre:
         out["prefill"] = pre
     return out
@@ -463,7 +492,7 @@ def run(args):
     if world == 1:
         del layers, wss
         torch.cuda.empty_cache()
-        extra = run_sections(args, hbm_peak, tc_peak, peak_kind)
+        extra = run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=not args.no_cpu_baseline)
     line = {
         "metric": DECODE_METRIC,
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,

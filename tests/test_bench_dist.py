@@ -60,3 +60,10 @@ def test_single_process_defaults():
         os.environ.pop(k, None)
     assert bench._dist() == (1, 0, 0)
     assert bench.max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
+
+
+def test_prefill_cpu_baseline_on_a_tiny_workload():
+    # the oracle's prefill rate reported beside each prefill section
+    cb = bench.cpu_baseline_prefill("tiny-decode", tokens=3)
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "tok/s"
+    assert cb["value"] > 0 and "first 3 tokens" in cb["sample"]
