@@ -131,3 +131,48 @@ def test_entry_points_reject_bad_arguments_before_launch():
     assert lib.moe_ffn_decode_static(C.byref(L), None, FAKE, None, None) == M.CODE["MOEQ_ERR_ARG"]
     assert lib.h32_rotate(None, None, 4, None, None) == M.CODE["MOEQ_ERR_ARG"]
     assert lib.moe_rmsnorm_bf16(FAKE, 1, 100, FAKE, None) == M.CODE["MOEQ_ERR_SHAPE"]
+
+
+def test_prefill_entry_points_reject_bad_arguments_before_launch():
+    lib = M.load()
+    L = _layer()
+    need = lib.moe_ffn_workspace(C.byref(L), 8, 2)
+    assert need > 0
+
+    def prefill(x=FAKE, T=8, residual=None, y=FAKE, ws=FAKE, ws_bytes=need, layer=L):
+        return lib.moe_ffn_prefill(C.byref(layer), x, T, residual, y, ws, ws_bytes, None, None, None)
+
+    assert prefill(layer=_layer(k=0)) == M.CODE["MOEQ_ERR_ARG"]       # the layer is validated first
+    assert prefill(T=-1) == M.CODE["MOEQ_ERR_SHAPE"]
+    assert prefill(T=0, x=None, y=None, ws=None) == 0                 # T = 0 enqueues nothing
+    assert prefill(x=None) == M.CODE["MOEQ_ERR_ARG"]
+    assert prefill(y=None) == M.CODE["MOEQ_ERR_ARG"]
+    assert prefill(x=FAKE + 8) == M.CODE["MOEQ_ERR_ALIGN"]
+    assert prefill(residual=FAKE + 4) == M.CODE["MOEQ_ERR_ALIGN"]
+    assert prefill(ws_bytes=need - 1) == M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert prefill(ws=None) == M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert prefill(ws=FAKE + 8) == M.CODE["MOEQ_ERR_WORKSPACE"]
+    # a larger T needs a larger workspace
+    assert lib.moe_ffn_workspace(C.byref(L), 9, 2) > need
+
+    # the layer stack: every layer validated, one H, workspace for the largest layer + the RMSNorm output
+    arr = (M.MoeqLayer * 2)(_layer(), _layer())
+    need3 = lib.moe_ffn_workspace(C.byref(L), 8, 3)
+    assert need3 > need
+
+    def stack(layers=arr, n=2, x=FAKE, T=8, r=FAKE, ws=FAKE, ws_bytes=need3):
+        return lib.moe_ffn_stack_prefill(layers, n, x, T, r, ws, ws_bytes, None, None)
+
+    assert stack(layers=None) == M.CODE["MOEQ_ERR_ARG"]
+    assert stack(n=0) == M.CODE["MOEQ_ERR_ARG"]
+    assert stack(T=-1) == M.CODE["MOEQ_ERR_SHAPE"]
+    assert stack(layers=(M.MoeqLayer * 2)(_layer(), _layer(k=0))) == M.CODE["MOEQ_ERR_ARG"]
+    wide = _layer(H=512)
+    wide.router = FAKE
+    wide.gate, wide.up, wide.down = _mat(2, 256, 512, 16), _mat(2, 256, 512, 16), _mat(3, 512, 256, 16)
+    assert M.moeq_validate_layer(wide) == 0
+    assert stack(layers=(M.MoeqLayer * 2)(_layer(), wide)) == M.CODE["MOEQ_ERR_SHAPE"]  # one H
+    assert stack(T=0, x=None, r=None, ws=None) == 0
+    assert stack(r=None) == M.CODE["MOEQ_ERR_ARG"]
+    assert stack(x=FAKE + 2) == M.CODE["MOEQ_ERR_ALIGN"]
+    assert stack(ws_bytes=need3 - 1) == M.CODE["MOEQ_ERR_WORKSPACE"]
