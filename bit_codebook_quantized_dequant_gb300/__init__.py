@@ -50,7 +50,8 @@ class MoeqLayer(C.Structure):
 
 class MoeqDebug(C.Structure):
     _fields_ = [(n, P) for n in ("xq", "xd", "logits", "idx", "p", "h", "hq", "hd", "o", "S_gate",
-                                 "S_up", "S_down", "trace")] + [("trace_cap", C.c_int)]
+                                 "S_up", "S_down", "trace")] + [("trace_cap", C.c_int),
+                                                                ("spin_limit", C.c_int)]
 
 
 TRACE_EVENTS = {1: "START", 2: "TAKE", 3: "TOPK", 4: "ISSUED", 5: "READY", 6: "DONE",

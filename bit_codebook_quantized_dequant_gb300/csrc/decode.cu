@@ -123,6 +123,7 @@ struct DecodeArgs {
   int nR, nSG, nDN, nSD;  // item counts that do not depend on the routing
   int route_idx;          // queue index of the routing item
   int route_base, n_ctr;  // counter word offsets (moeq_layout.h)
+  uint32_t spin;          // polls of each wait on another CTA before it gives up
 };
 
 template <int COLS>
@@ -259,7 +260,7 @@ template <int COLS>
 __device__ void fetch_route(const DecodeArgs& a, DecodeSmem<COLS>& sm, int lane) {
   constexpr int RL = route_lines(COLS);
   const uint32_t* rec = a.ctr + a.route_base + kCtrLine * RL * (blockIdx.x % kRouteCopies);
-  if (lane == 0 && !spin_until_geq(rec + kCtrLine * (RL - 1) + kRouteFlag, 1u))
+  if (lane == 0 && !spin_until_geq(rec + kCtrLine * (RL - 1) + kRouteFlag, 1u, a.spin))
     set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
   __syncwarp();
   if constexpr (COLS == 1) {
@@ -301,7 +302,7 @@ __device__ void route_item(const DecodeArgs& a, DecodeSmem<COLS>& sm, int bar, i
   constexpr int NPL = kMaxE / (32 * WPC);   // logits per lane
   const int warp = t >> 5, lane = t & 31;
   const int col = warp / WPC, sub = warp % WPC;
-  if (t == 0 && !spin_until_geq(&a.ctr[kCtrRouter], static_cast<uint32_t>(a.nR)))
+  if (t == 0 && !spin_until_geq(&a.ctr[kCtrRouter], static_cast<uint32_t>(a.nR), a.spin))
     set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
   named_bar(bar, kGroupThreads);
   float l[NPL];
@@ -508,7 +509,7 @@ __device__ void issue_unit(const DecodeArgs& a, DecodeSmem<COLS>& sm, int s, con
   const int e = un.kind == U_SDOWN ? 0 : uw_expert(w);
   bulk_g2s(sm.stage_cb[s], D.cb + static_cast<size_t>(e) * D.cb_stride, 16, bar);
   const uint32_t need = static_cast<uint32_t>(a.I / 32) * static_cast<uint32_t>(__popc(uw_mask(w)));
-  if (!spin_until_geq(&a.ctr[kCtrHqDone + kCtrLine * un.slot], need))
+  if (!spin_until_geq(&a.ctr[kCtrHqDone + kCtrLine * un.slot], need, a.spin))
     set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
   asm volatile("fence.proxy.async.global;" ::: "memory");
   bulk_g2s(st + mp.cb, a.hq + static_cast<size_t>(un.slot) * COLS * a.I, hqb, bar);
@@ -1161,7 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const DecodeArgs a) {
     if (warp == 0) {
       if (!sm.have_route) fetch_route<COLS>(a, sm, lane);
       const uint32_t target = static_cast<uint32_t>(a.nSD + sm.nu * per);
-      if (lane == 0 && !spin_until_geq(&a.ctr[kCtrDownDone], target))
+      if (lane == 0 && !spin_until_geq(&a.ctr[kCtrDownDone], target, a.spin))
         set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
       __syncwarp();
     }
@@ -1234,6 +1235,12 @@ void fill_args(DecodeArgs& a, const moeq_layer* L, int cols, const uint16_t* x, 
   a.obuf = reinterpret_cast<float*>(w + wl.obuf);
   a.status = dev_status;
   if (dbg) a.dbg = *dbg;
+  // a caller's limit for the cross-CTA waits, one column only: with four
+  // columns a routing record read before it is complete could name units
+  // without columns, so the q=4 kernel keeps the default
+  a.spin = kSpinLimit;
+  if (cols == 1 && dbg && dbg->spin_limit != 0)
+    a.spin = dbg->spin_limit < 0 ? 0u : static_cast<uint32_t>(dbg->spin_limit);
   a.nR = L->E / kRouterRows;
   a.nSG = a.has_shared ? L->I / (2 * kGuRows) : 0;
   a.nSD = a.has_shared ? L->H / kDownRows : 0;
@@ -1327,7 +1334,8 @@ extern "C" int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, 
 // The decode's scratch (counters, routing record, logits, quantized h,
 // per-expert outputs) lives here instead of in a caller workspace, for
 // callers that cannot allocate device memory. One array per device (the
-// module's copy on each device); its address is looked up once per device.
+// module's copy on each device); its address is looked up per device and
+// per CUDA context.
 namespace moeq {
 namespace {
 
@@ -1337,15 +1345,47 @@ static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];
 
-// Address of this device's scratch (the current device), or nullptr.
+// Unique id of the current CUDA context (driver entry points looked up through
+// the runtime; 0 when unavailable).
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+// Address of the current device's scratch, or nullptr. Looked up again when
+// the current context differs from the one of the cached address (a device
+// reset reloads the module in a new primary context).
 void* static_scratch(int device) {
   if (device < 0 || device >= kMaxDevices) return nullptr;
+  cudaFree(nullptr);  // make sure the device's primary context is current
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[device]) {
+  if (!g_scratch_ptr[device] || g_scratch_ctx[device] != ctx || ctx == 0) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
     g_scratch_ptr[device] = p;
+    g_scratch_ctx[device] = ctx;
   }
   return g_scratch_ptr[device];
 }

@@ -104,8 +104,9 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 }
 
 // Bounded spin until *p >= target (acquire). false when the limit ran out.
-__device__ __forceinline__ bool spin_until_geq(const uint32_t* p, uint32_t target) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+__device__ __forceinline__ bool spin_until_geq(const uint32_t* p, uint32_t target,
+                                               uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (ld_acquire(p) >= target) return true;
     __nanosleep(i < 4 ? 32 : 200);
   }

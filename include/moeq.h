@@ -107,6 +107,11 @@ typedef struct {
                                    trace_cap x 2] (roles: expansion, activation producer,
                                    MMA issue, epilogue) */
   int trace_cap;                /* events per (CTA, role) */
+  int spin_limit;               /* decode only: polls of each wait on another CTA's progress
+                                   before it gives up with MOEQ_ERR_DEVICE_TIMEOUT; 0 = the
+                                   default (2^20 polls of up to ~0.2 us), < 0 = give up at
+                                   once (tests of the timeout path); the q=4 entry point
+                                   always uses the default */
 } moeq_debug;
 
 /* Timeline events of moe_ffn_decode and moe_ffn_verify_q4 (role 0 = compute
@@ -196,8 +201,9 @@ int moe_ffn_decode(const moeq_layer* L, const uint16_t* x, float* y, void* ws, s
  *   - Every call on a device uses the same scratch: calls that may overlap in
  *     time (different streams, or different host threads without ordering)
  *     race on it and give wrong results. Order them, e.g. on one stream.
- *   - The first call on a device looks up the scratch's address (host side,
- *     no allocation); make that first call before any stream capture.
+ *   - The first call on a device (and the first after the device's context
+ *     was reset) looks up the scratch's address (host side, no allocation);
+ *     make that first call before any stream capture.
  * Results are those of moe_ffn_decode; no debug output. */
 int moe_ffn_decode_static(const moeq_layer* L, const uint16_t* x, float* y, int32_t* dev_status,
                           moeq_stream stream);

@@ -90,3 +90,43 @@ def test_decode_repeatable_and_workspace_reused():
     n_ctr = 32 * (4 + ns) + 32 * 16   # counter lines, then the routing record copies
     ctr = ws.buf[: 4 * n_ctr].view(torch.int32).cpu().numpy()
     assert not ctr.any()
+
+
+def test_decode_wait_timeout_reported_then_next_calls_exact():
+    """A cross-CTA wait that gives up at once (spin_limit < 0) ends the call
+    with MOEQ_ERR_DEVICE_TIMEOUT in the status word and no device error; the
+    last CTA still resets the workspace counters, so the next call on the same
+    workspace and a call of the library-owned-scratch entry point give the bits
+    of a fresh workspace."""
+    cfg = _cfg("tiny-decode", shared_fmt=4, k=3)
+    seed = S.workload_seed("tiny-decode") + 5
+    dl = build_layer(seed, 0, cfg)
+    xs = S.tokens(seed, cfg, 2)
+    H = cfg["H"]
+
+    def call(ws, x, dbg=None):
+        y = torch.zeros(H, dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        M.moe_ffn_decode(dl.desc(), to_dev_u16(x), y, ws.ptr, ws.nbytes, st, dbg)
+        torch.cuda.synchronize()
+        return y.cpu().numpy(), st.item()
+
+    y_ref, st_ref = call(Workspace(dl, 0), xs[1])
+    assert st_ref == 0
+    ws = Workspace(dl, 0)
+    dbg = M.MoeqDebug()
+    dbg.spin_limit = -1
+    _, st_to = call(ws, xs[0], dbg)
+    assert st_to == M.CODE["MOEQ_ERR_DEVICE_TIMEOUT"]
+    ns = cfg["k"] + 1
+    n_ctr = 32 * (4 + ns) + 32 * 16
+    assert not ws.buf[: 4 * n_ctr].view(torch.int32).cpu().numpy().any()
+    y, st = call(ws, xs[1])
+    assert st == 0
+    np.testing.assert_array_equal(y, y_ref)
+    y_s = torch.zeros(H, dtype=torch.float32, device="cuda")
+    st_s = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_ffn_decode_static(dl.desc(), to_dev_u16(xs[1]), y_s, st_s)
+    torch.cuda.synchronize()
+    assert st_s.item() == 0
+    np.testing.assert_array_equal(y_s.cpu().numpy(), y_ref)
