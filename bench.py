@@ -246,6 +246,109 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def capture_steps(step, first, n, stream, chunk=64):
+    """CUDA graphs of steps first .. first + n - 1 (chunks of `chunk` steps),
+    each step enqueued by step(i, stream)."""
+    import torch
+    graphs, i = [], first
+    while i < first + n:
+        m = min(chunk, first + n - i)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(m):
+                step(i + j, stream)
+        graphs.append(g)
+        i += m
+    return graphs
+
+
+def replay(graphs, stream):
+    """Replays the graphs on `stream` (a graph launches on the current stream)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+
+
+def _abs_weights(m, e):
+    """|w| of expert e of an oracle matrix, fp32 (a tolerance, not a result; cpu leg)."""
+    import oracle as O
+    codes = O.unpack(m.fmt, m.rows, m.cols, m.codes[e])
+    sv = O.scale_values(m.fmt, m.scales[e]).astype(np.float32).reshape(m.rows, m.cols // 32)
+    return np.abs(np.repeat(sv, 32, axis=1) * m.cb[e].astype(np.float32)[codes])
+
+
+def oracle_parity(L, x_rows, ys, hqs, hds):
+    """The oracle (cpu leg) on sampled tokens against the GPU's outputs ys and
+    quantized h (hqs, hds: [tokens, slots, I] / [tokens, slots, I/32]):
+    |y - y_oracle| <= 2e-3 B + D with B = sum_slot p sum_k |w_down| |h~| (the
+    GPU's h~) and D = sum_slot p sum_k |w_down| |h~ - h~_oracle|, and the
+    relative L2 error. Returns (ok, worst err / bound, worst relative L2)."""
+    import oracle as O
+    worst, rel_worst, ok = 0.0, 0.0, True
+    for t in range(len(x_rows)):
+        yo, tr = O.ffn_decode(L, x_rows[t], trace=True)
+        slots = [(L.down, int(e)) for e in tr["idx"]]
+        if L.shared is not None:
+            slots.append((L.shared[2], 0))
+        w = list(tr["p"]) + ([1.0] if L.shared is not None else [])
+        B = np.zeros(L.H)
+        D = np.zeros(L.H)
+        for s, (m, e) in enumerate(slots):
+            hg = hqs[t][s].astype(np.float64) * np.repeat(O.f16_array_to_f64(hds[t][s]), 32)
+            ho = tr["hq"][s].astype(np.float64) * np.repeat(O.f16_array_to_f64(tr["hd"][s]), 32)
+            A = _abs_weights(m, e)
+            B += w[s] * (A @ np.abs(hg).astype(np.float32)).astype(np.float64)
+            D += w[s] * (A @ np.abs(hg - ho).astype(np.float32)).astype(np.float64) * (1 + 1e-5)
+        y = np.asarray(ys[t], dtype=np.float64)
+        err = np.abs(y - yo)
+        lim = 2e-3 * B + D
+        worst = max(worst, float(np.max(err / np.maximum(lim, 1e-300))))
+        rel = float(np.linalg.norm(y - yo) / max(np.linalg.norm(yo), 1e-300))
+        rel_lim = 1e-4 + float(np.linalg.norm(D) / max(np.linalg.norm(yo), 1e-300))
+        rel_worst = max(rel_worst, rel / rel_lim)
+        ok = ok and bool(np.all(err <= lim)) and rel <= rel_lim
+    return ok, worst, rel_worst
+
+
+def gpu_decode_rows(dl, ws, x_rows, cfg):
+    """Sampled tokens through the decode with its debug outputs: y, hq, hd per token."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300.workload import Debug, to_dev_u16
+    H, I = cfg["H"], cfg["I"]
+    ns = cfg["k"] + (1 if cfg["shared_fmt"] else 0)
+    ys, hqs, hds = [], [], []
+    for t in range(len(x_rows)):
+        d = Debug(cfg, 1)
+        y = torch.zeros(H, dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        M.moe_ffn_decode(dl.desc(), to_dev_u16(x_rows[t]), y, ws.ptr, ws.nbytes, st, d.struct)
+        torch.cuda.synchronize()
+        assert st.item() == 0, f"device status {st.item()}"
+        g = d.numpy()
+        ys.append(y.cpu().numpy())
+        hqs.append(g["hq"].reshape(ns, I))
+        hds.append(g["hd"].reshape(ns, I // 32))
+    return ys, hqs, hds
+
+
+def decode_parity_after(dl, ws, xs_host, cfg, seed, ntok=4):
+    """After the timed steps: the first sampled tokens of the cpu leg (layer 0)
+    through the decode once more, against the oracle's outputs."""
+    from oracle import workload as W
+    x = xs_host[:ntok]
+    ys, hqs, hds = gpu_decode_rows(dl, ws, x, cfg)
+    idx, _ = W.route(seed, 0, cfg, x)
+    L = W.layer(seed, 0, cfg, {int(e) for r in idx for e in r})
+    ok, worst, rel = oracle_parity(L, x, ys, hqs, hds)
+    return {"tokens": ntok, "layer": 0, "ok": ok, "max_err_over_limit": worst,
+            "max_rel_l2_over_limit": rel,
+            "check": "y of sampled tokens against the fp64 oracle: |err| <= 2e-3 B + D, relative L2 "
+                     "<= 1e-4 + |D|/|y| (B: sum_slot p |w_down| |h~|; D: the same on the difference "
+                     "of the GPU's and the oracle's quantized h)"}
+
+
 def _timed(fn, warmup, steps, stream):
     import torch
     for i in range(warmup):
@@ -260,7 +363,49 @@ def _timed(fn, warmup, steps, stream):
     return e0.elapsed_time(e1) / steps
 
 
-def bench_verify(args, hbm_peak, peak_kind):
+def verify_parity_after(dl, ws, X, cfg, seed):
+    """After the timed calls: one batch of 4 columns through the q=4 call once
+    more, each column and the dense projection against the oracle."""
+    import torch
+    import oracle as O
+    from oracle import workload as W
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300.workload import Debug, to_dev_u16
+    H, I = cfg["H"], cfg["I"]
+    ns = cfg["k"] + (1 if cfg["shared_fmt"] else 0)
+    d = Debug(cfg, 4)
+    y = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
+    yd = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_ffn_verify_q4(dl.desc(), dl.dense.desc(), to_dev_u16(X), y, yd, ws.ptr, ws.nbytes, st, d.struct)
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    g = d.numpy()
+    ys = y.cpu().numpy().reshape(4, H)
+    hq = g["hq"].reshape(4, ns, I)
+    hd = g["hd"].reshape(4, ns, I // 32)
+    idx, _ = W.route(seed, 0, cfg, X)
+    L = W.layer(seed, 0, cfg, {int(e) for r in idx for e in r})
+    ok, worst, rel = oracle_parity(L, X, list(ys), list(hq), list(hd))
+    # dense projection: |err| <= 2e-3 sum |w_dense| |x~| per row
+    Dm = W.dense(seed, 0, cfg)
+    _, yd_ref = O.ffn_verify_q4(L, Dm, X)
+    A = _abs_weights(Dm, 0)
+    yd = yd.cpu().numpy().reshape(4, H)[:, :Dm.rows]
+    xq, xd = g["xq"].reshape(4, H), g["xd"].reshape(4, H // 32)
+    for c in range(4):
+        xt = np.abs(xq[c].astype(np.float32) * np.repeat(O.f16_array_to_f64(xd[c]).astype(np.float32), 32))
+        bound = 2e-3 * (A @ xt).astype(np.float64)
+        err = np.abs(yd[c] - yd_ref[c])
+        worst = max(worst, float(np.max(err / np.maximum(bound, 1e-300))))
+        ok = ok and bool(np.all(err <= bound))
+    return {"batches": 1, "columns": 4, "layer": 0, "ok": ok, "max_err_over_limit": worst,
+            "max_rel_l2_over_limit": rel,
+            "check": "each column's y against the fp64 oracle as in the decode section; y_dense "
+                     "within 2e-3 sum |w| |x~| per row"}
+
+
+def bench_verify(args, hbm_peak, peak_kind, cpu=False):
     """q=4 verification: 4 columns per call through moe_ffn_verify_q4, cycling
     over 2 seeded layer replicas (each with its dense projection)."""
     import torch
@@ -282,16 +427,31 @@ def bench_verify(args, hbm_peak, peak_kind):
     y = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
     yd = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
 
-    def step(i):
+    def step(i, s):
         r = i % R
         M.moe_ffn_verify_q4(descs[r], dds[r], xs.data_ptr() + (i % nb) * 4 * H * 2, y, yd,
-                            wss[r].ptr, wss[r].nbytes, st, None, stream)
+                            wss[r].ptr, wss[r].nbytes, st, None, s)
 
     steps = max(args.steps // 4, 50)
-    ms = _timed(step, args.warmup, steps, stream)
+    for i in range(args.warmup):
+        step(i, stream)
+    torch.cuda.synchronize()
+    graphs = capture_steps(step, args.warmup, steps, stream)
+    replay(graphs, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(graphs, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del graphs
     assert st.item() == 0, f"device status {st.item()}"
+    parity = None
+    if cpu:
+        parity = verify_parity_after(layers[0], wss[0], X[:4], cfg, seed)
     # distinct experts per call (routing of the same columns, outside the timed region)
     distinct = []
     idx = torch.zeros(4 * cfg["k"], dtype=torch.int32, device="cuda")
@@ -315,10 +475,42 @@ def bench_verify(args, hbm_peak, peak_kind):
                                             "bit_codebook_quantized_dequant_gb300/csrc/decode.cu"),
                         "peak_source": f"{peak_kind} hbm_gbs",
                         "algorithmic_bytes_per_launch": per_call},
-           "gpu_launches": steps}
+           "gpu_launches": steps, "launch": "CUDA graph replay",
+           "parity_after": parity}
     del layers, wss
     torch.cuda.empty_cache()
     return out
+
+
+def prefill_parity_after(dl, ws, X_host, X_dev, y, cfg, seed, T):
+    """After the timed calls: the prefill once more with its quantized h
+    recorded, then sampled tokens' y against the oracle (as in the decode
+    section; the prefill's h comes from tensor-core part products)."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from oracle import workload as W
+    H, I = cfg["H"], cfg["I"]
+    ns = cfg["k"] + (1 if cfg["shared_fmt"] else 0)
+    hq = torch.zeros(T * ns * I, dtype=torch.int8, device="cuda")
+    hd = torch.zeros(T * ns * (I // 32), dtype=torch.int16, device="cuda")
+    dbg = M.MoeqDebug(hq=hq.data_ptr(), hd=hd.data_ptr())
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_ffn_prefill(dl.desc(), X_dev, T, None, y, ws.ptr, ws.nbytes, st, dbg)
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    sample = [0, T // 2 + 1, T - 1]
+    idx_t = torch.as_tensor(sample, dtype=torch.long, device="cuda")
+    ys = y.view(T, H).index_select(0, idx_t).cpu().numpy()
+    hqs = hq.view(T, ns, I).index_select(0, idx_t).cpu().numpy()
+    hds = hd.view(T, ns, I // 32).index_select(0, idx_t).cpu().numpy().view(np.uint16)
+    x = X_host[sample]
+    idx, _ = W.route(seed, 0, cfg, x)
+    L = W.layer(seed, 0, cfg, {int(e) for r in idx for e in r})
+    ok, worst, rel = oracle_parity(L, x, list(ys), list(hqs), list(hds))
+    del hq, hd
+    return {"tokens": sample, "layer": 0, "ok": ok, "max_err_over_limit": worst,
+            "max_rel_l2_over_limit": rel,
+            "check": "y of sampled tokens against the fp64 oracle as in the decode section"}
 
 
 def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind, cpu=False):
@@ -331,7 +523,8 @@ def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind, cpu=False):
     seed = S.workload_seed(name)
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 2, T)
-    X = to_dev_u16(S.tokens(seed, cfg, T))
+    X_host = S.tokens(seed, cfg, T)
+    X = to_dev_u16(X_host)
     y = torch.zeros(T * cfg["H"], dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -346,20 +539,35 @@ def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind, cpu=False):
     fl = prefill_flops(cfg, T)
     tflops = fl / (ms * 1e-3) / 1e12
     wbytes = dl.weight_bytes()
+    hbm_gbs = wbytes / (ms * 1e-3) / 1e9
+    tensor = {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+              "frac": tflops / tc_peak,
+              "traffic": _traffic(f"prefill {name} gemm",
+                                  "bit_codebook_quantized_dequant_gb300/csrc/gemm_tc.cu"),
+              "traffic_scope": "DRAM bytes of the gate, up and down tensor-core "
+                               "launches of one call (routed experts)",
+              "peak_source": f"{peak_kind} bf16_tflops (the prefill contraction runs "
+                             "as bf16 part products on the tensor cores)",
+              "algorithmic_flops_per_launch": fl}
+    hbm = {"bound": "hbm", "achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s",
+           "frac": hbm_gbs / hbm_peak, "traffic": None,
+           "peak_source": f"{peak_kind} hbm_gbs",
+           "algorithmic_bytes_per_launch": wbytes}
+    # the layer's bound: its FLOP per weight byte against the bf16 ridge
+    ridge = tc_peak * 1e12 / (hbm_peak * 1e9)
+    hbm_bound = fl / wbytes < ridge
     out = {"metric": "prefill tok/s (one layer)", "value": T / (ms * 1e-3), "unit": "tok/s",
            "ms_per_call": ms, "calls": steps, "tokens": T,
-           "workload": name + f": T={T}, all 256 experts' weights read once",
-           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                        "frac": tflops / tc_peak,
-                        "traffic": _traffic(f"prefill {name} gemm",
-                                            "bit_codebook_quantized_dequant_gb300/csrc/gemm_tc.cu"),
-                        "traffic_scope": "DRAM bytes of the gate, up and down tensor-core "
-                                         "launches of one call (routed experts)",
-                        "peak_source": f"{peak_kind} bf16_tflops (the prefill contraction runs "
-                                       "as bf16 part products on the tensor cores)",
-                        "algorithmic_flops_per_launch": fl,
-                        "hbm_frac_weights": wbytes / (ms * 1e-3) / 1e9 / hbm_peak},
+           "workload": name + f": T={T}, one layer, all 256 experts' weights read once",
+           "flop_per_weight_byte": fl / wbytes, "ridge_flop_per_byte": ridge,
+           "roofline": hbm if hbm_bound else tensor,
+           "roofline_other": tensor if hbm_bound else hbm,
            "gpu_launches_per_call": prefill_launches(cfg)}
+    if cpu:
+        try:
+            out["parity_after"] = prefill_parity_after(dl, ws, X_host, X, y, cfg, seed, T)
+        except Exception as e:  # reported, not hidden
+            out["parity_after"] = {"ok": False, "error": repr(e)}
     del dl, ws
     torch.cuda.empty_cache()
     if cpu:
@@ -370,13 +578,121 @@ def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind, cpu=False):
     return out
 
 
+def bench_stack(args, T, nlayers, tc_peak, peak_kind):
+    """The 43-layer stack of the prefill workload: T tokens through nlayers
+    independently seeded layers (moe_ffn_stack_prefill: RMSNorm, FFN and
+    residual per layer), all layers resident in HBM."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, to_dev_u16
+    name = "prefill-43-layer-stack"
+    cfg = S.WORKLOADS[name]
+    seed = S.workload_seed(name)
+    layers = [build_layer(seed, l, cfg) for l in range(nlayers)]
+    descs = [dl.desc() for dl in layers]
+    ws = Workspace(layers[0], 3, T)
+    X = to_dev_u16(S.tokens(seed, cfg, T))
+    r = torch.zeros(T * cfg["H"], dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        M.moe_ffn_stack_prefill(descs, X, T, r, ws.ptr, ws.nbytes, st, stream)
+
+    ms = _timed(step, 1, 1, stream)
+    assert st.item() == 0, f"device status {st.item()}"
+    r1 = r.clone()
+    step(0)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(r, r1))
+    fl = nlayers * prefill_flops(cfg, T)
+    tflops = fl / (ms * 1e-3) / 1e12
+    wbytes = sum(dl.weight_bytes() for dl in layers)
+    out = {"metric": f"prefill tok/s ({nlayers}-layer stack)", "value": T / (ms * 1e-3),
+           "unit": "tok/s", "ms_per_call": ms, "calls": 1, "tokens": T, "layers": nlayers,
+           "workload": f"{name}: T={T}, {nlayers} independently seeded layers "
+                       f"({wbytes / 1e9:.1f} GB resident), RMSNorm + FFN + residual per layer",
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                        "frac": tflops / tc_peak, "traffic": None,
+                        "peak_source": f"{peak_kind} bf16_tflops",
+                        "algorithmic_flops_per_launch": fl},
+           "parity_after": {"repeat_bit_equal": same,
+                            "check": "the stack's output after the timed call equals a second "
+                                     "call's bit for bit; the stack's oracle parity (chain, "
+                                     "teacher-forced per layer) is a GPU test"}}
+    del ws, r, r1
+    torch.cuda.empty_cache()
+    dec = bench_stack_decode(args, layers, cfg, seed)
+    del layers
+    torch.cuda.empty_cache()
+    return out, dec
+
+
+def bench_stack_decode(args, layers, cfg, seed):
+    """One decode token at a time through the whole stack (moe_ffn_stack_decode:
+    RMSNorm, decode and residual per layer), steps replayed from CUDA graphs."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Workspace, to_dev_u16
+    nl = len(layers)
+    descs = [dl.desc() for dl in layers]
+    ws = Workspace(layers[0], 4)
+    H = cfg["H"]
+    ntok = 16
+    xs = to_dev_u16(S.tokens(seed, cfg, ntok, start=4096))
+    r = torch.zeros(H, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(i, s):
+        M.moe_ffn_stack_decode(descs, xs.data_ptr() + (i % ntok) * H * 2, r, ws.ptr, ws.nbytes, st, s)
+
+    warm, steps = 3, 8
+    for i in range(warm):
+        step(i, stream)
+    torch.cuda.synchronize()
+    graphs = capture_steps(step, warm, steps, stream, chunk=8)
+    replay(graphs, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(graphs, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    assert st.item() == 0, f"device status {st.item()}"
+    r_graph = r.clone()
+    step(warm + steps - 1, stream)  # the last timed token again, launched on the stream
+    torch.cuda.synchronize()
+    same = bool(torch.equal(r, r_graph))
+    del graphs
+    hbm_peak, _, peak_kind = _peaks()
+    per_tok = nl * algorithmic_bytes_decode(cfg)
+    achieved = per_tok / (ms * 1e-3) / 1e9
+    return {"metric": f"decode tok/s ({nl}-layer stack, b=1)", "value": 1.0 / (ms * 1e-3),
+            "unit": "tok/s", "ms_per_token": ms, "tokens_timed": steps, "layers": nl,
+            "workload": f"prefill-43-layer-stack layers (decode-b1 shapes), one token through all "
+                        f"{nl} layers per step: RMSNorm + decode + fp32 residual per layer",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": per_tok},
+            "gpu_launches_per_token": 2 * nl + 1, "launch": "CUDA graph replay",
+            "parity_after": {"repeat_bit_equal": same,
+                             "check": "the last timed token through the stack again, launched on a "
+                                      "stream, equals the graph's output bit for bit; the stack's "
+                                      "oracle parity is a GPU test"}}
+
+
 def run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=False):
     """The q=4 verification and prefill sections named in --sections (cpu: add
     the oracle's prefill rate on the host to each prefill section)."""
     sec = args.sections.split(",")
     out = {}
     if "verify" in sec:
-        out["verify_q4"] = bench_verify(args, hbm_peak, peak_kind)
+        out["verify_q4"] = bench_verify(args, hbm_peak, peak_kind, cpu)
     pre = []
     if "prefill" in sec or "prefill3" in sec:
         pre.append(bench_prefill(args, "prefill-h32-fp4", args.prefill_tokens or 2048, tc_peak, hbm_peak,
@@ -386,6 +702,9 @@ def run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=False):
                                  hbm_peak, peak_kind, cpu))
     if pre:
         out["prefill"] = pre
+    if "stack" in sec:
+        out["prefill_stack"], out["decode_stack"] = bench_stack(
+            args, args.prefill_tokens or 32512, args.stack_layers, tc_peak, peak_kind)
     return out
 
 
@@ -423,51 +742,95 @@ def run(args):
     stream = torch.cuda.current_stream()
     xbase, xstride = xs.data_ptr(), H * 2
 
-    def step(i):
+    def step(i, s):
         r = i % R
         M.moe_ffn_decode(descs[r], xbase + (i % ntok) * xstride, y, wss[r].ptr, wss[r].nbytes, st,
-                         None, stream)
+                         None, s)
 
+    # W warm-up steps launched on the stream, then the K timed steps replayed
+    # from CUDA graphs (captured and replayed once, untimed, before timing)
+    stream = torch.cuda.Stream()
     for i in range(args.warmup):
-        step(i)
+        step(i, stream)
     torch.cuda.synchronize()
+    graphs = capture_steps(step, args.warmup, args.steps, stream)
+    replay(graphs, stream)
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
     if dist:
         dist.barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         torch.cuda.synchronize()
         ev0.record(stream)
-        for i in range(args.steps):
-            step(args.warmup + i)
+        replay(graphs, stream)
         ev1.record(stream)
         torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     assert st.item() == 0, f"device status {st.item()}"
+    del graphs
 
-    # end to end through the same entry point with host buffers: pinned x in,
-    # y out, both inside the timed region
+    # end to end through the same entry point with host buffers: per step the
+    # token's x from pinned memory to the device, the decode, and y back to
+    # pinned memory, on three streams with two buffers each so that the copies
+    # of neighbouring steps overlap the decode; captured and replayed like the
+    # device-timed steps
     x_pin = torch.from_numpy(xs_host.view(np.int16)).pin_memory()
     y_pin = torch.empty((args.steps, H), dtype=torch.float32).pin_memory()
-    xdev = torch.empty(H, dtype=torch.int16, device="cuda")
+    xdev = torch.empty((2, H), dtype=torch.int16, device="cuda")
+    ydev = torch.empty((2, H), dtype=torch.float32, device="cuda")
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("x", "used", "y", "out")}
 
-    def step_e2e(i):
-        r = i % R
-        xdev.copy_(x_pin[i % ntok], non_blocking=True)
-        M.moe_ffn_decode(descs[r], xdev, y, wss[r].ptr, wss[r].nbytes, st, None, stream)
-        y_pin[i % args.steps].copy_(y, non_blocking=True)
+    def e2e_chunk(first, n, s):
+        s_in.wait_stream(s)
+        s_out.wait_stream(s)
+        for j in range(n):
+            i, b = first + j, (first + j) % 2
+            r = i % R
+            if j >= 2:
+                s_in.wait_event(ev["used"][b])
+            with torch.cuda.stream(s_in):
+                xdev[b].copy_(x_pin[i % ntok], non_blocking=True)
+                ev["x"][b].record(s_in)
+            s.wait_event(ev["x"][b])
+            if j >= 2:
+                s.wait_event(ev["out"][b])
+            M.moe_ffn_decode(descs[r], xdev[b], ydev[b], wss[r].ptr, wss[r].nbytes, st, None, s)
+            ev["used"][b].record(s)
+            ev["y"][b].record(s)
+            s_out.wait_event(ev["y"][b])
+            with torch.cuda.stream(s_out):
+                y_pin[i - args.warmup].copy_(ydev[b], non_blocking=True)
+                ev["out"][b].record(s_out)
+        s.wait_stream(s_in)
+        s.wait_stream(s_out)
 
-    for i in range(args.warmup):
-        step_e2e(i)
+    egraphs, i0 = [], args.warmup
+    while i0 < args.warmup + args.steps:
+        m = min(64, args.warmup + args.steps - i0)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_chunk(i0, m, stream)
+        egraphs.append(g)
+        i0 += m
+    replay(egraphs, stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
-        step_e2e(i)
+    replay(egraphs, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1)
+    assert st.item() == 0, f"device status {st.item()}"
+    # the end-to-end outputs are those of the device-timed path
+    for i in range(min(4, args.steps)):
+        step(args.warmup + i, stream)
+        torch.cuda.synchronize()
+        assert torch.equal(y.cpu(), y_pin[i]), "end-to-end output differs"
+    del egraphs
 
     if dist:
         ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, device="cuda")
@@ -483,9 +846,11 @@ def run(args):
     value = job_throughput(world, args.steps, ms)
     e2e = job_throughput(world, args.steps, ms_e2e)
     cpu = None
+    parity_after = None
     if world == 1 and not args.no_cpu_baseline:
         tps, sample, _ = cpu_baseline(DECODE_WORKLOAD, 20)
         cpu = {"value": tps, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample}
+        parity_after = decode_parity_after(layers[0], wss[0], xs_host, cfg, seed, ntok=4)
     traffic = _traffic("ffn_kernel<1>", "bit_codebook_quantized_dequant_gb300/csrc/decode.cu")
     wbytes = R * layers[0].weight_bytes()
     extra = {}
@@ -502,7 +867,9 @@ def run(args):
         "config": {"workload": WORKLOAD, "replicas": R,
                    "l2": f"inputs larger than L2: {R} independently seeded layer replicas "
                          f"({wbytes / 1e9:.1f} GB), cycled per step",
-                   "tokens": ntok},
+                   "tokens_timed": world * args.steps,
+                   "token_pool": ntok,
+                   "launch": "K steps replayed from CUDA graphs (stream-launched warm-up before)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs",
@@ -512,6 +879,7 @@ def run(args):
                 "d2h_bytes_per_step": H * 4},
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
+        "parity_after": parity_after,
     }
     line.update(extra)
     print(json.dumps(line))
@@ -527,9 +895,10 @@ def main():
     ap.add_argument("--replicas", type=int, default=8)
     ap.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sections", default="decode,verify,prefill",
-                    help="comma list of decode, verify, prefill (= prefill3,prefill4); "
+    ap.add_argument("--sections", default="decode,verify,prefill,stack",
+                    help="comma list of decode, verify, prefill (= prefill3,prefill4), stack; "
                          "without decode only the named sections run (profiling)")
+    ap.add_argument("--stack-layers", type=int, default=43)
     ap.add_argument("--prefill-tokens", type=int, default=0,
                     help="tokens of the prefill sections (default: the workloads' 2048 and 32512); "
                          "smaller counts for profiling")

@@ -15,7 +15,7 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoeq.so")
 
-MOEQ_FP2, MOEQ_FP3, MOEQ_FP4 = 2, 3, 4
+MOEQ_FP2, MOEQ_FP3, MOEQ_FP4, MOEQ_BF16 = 2, 3, 4, 16
 STATUS = {
     0: "MOEQ_OK", -1: "MOEQ_ERR_ARG", -2: "MOEQ_ERR_SHAPE", -3: "MOEQ_ERR_ALIGN",
     -4: "MOEQ_ERR_FORMAT", -5: "MOEQ_ERR_CODEBOOK_MISSING", -6: "MOEQ_ERR_CODEBOOK_TRUNCATED",
@@ -95,6 +95,8 @@ def _declare(L):
         "moe_ffn_prefill": (i, [C.POINTER(MoeqLayer), P, i, P, P, P, sz, P, C.POINTER(MoeqDebug),
                                 P]),
         "moe_ffn_stack_prefill": (i, [P, i, P, i, P, P, sz, P, P]),
+        "moe_ffn_stack_decode": (i, [P, i, P, P, P, sz, P, P]),
+        "moe_quantize_expert": (i, [i, i, i, P, P, P, P, P, sz, P, P]),
         "h32_rotate": (i, [P, P, i, P, P]),
         "moe_rmsnorm_bf16": (i, [P, i, i, P, P]),
         "moeq_version": (C.c_char_p, []),
@@ -110,7 +112,8 @@ def _declare(L):
 EXPORTED = ["moeq_packed_bytes", "moeq_validate_layer", "moe_ffn_workspace",
             "moe_ffn_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_ffn_decode",
             "moe_ffn_decode_static",
-            "moe_ffn_verify_q4", "moe_ffn_prefill", "moe_ffn_stack_prefill", "h32_rotate",
+            "moe_ffn_verify_q4", "moe_ffn_prefill", "moe_ffn_stack_prefill", "moe_ffn_stack_decode",
+            "moe_quantize_expert", "h32_rotate",
             "moe_rmsnorm_bf16",
             "moeq_version", "moeq_synth_codes", "moeq_synth_scales"]
 
@@ -195,6 +198,20 @@ def moe_ffn_prefill(layer: MoeqLayer, x, T, residual, y, ws, ws_bytes, dev_statu
     return _check("moe_ffn_prefill", load().moe_ffn_prefill(
         C.byref(layer), _ptr(x), T, _ptr(residual), _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status),
         C.byref(dbg) if dbg is not None else None, _stream(stream)))
+
+
+def moe_quantize_expert(fmt, rows, cols, w, codes_u8, scales, codebook, ws, ws_bytes, dev_status=None,
+                        stream=None):
+    return _check("moe_quantize_expert", load().moe_quantize_expert(
+        fmt, rows, cols, _ptr(w), _ptr(codes_u8), _ptr(scales), _ptr(codebook), _ptr(ws), ws_bytes,
+        _ptr(dev_status), _stream(stream)))
+
+
+def moe_ffn_stack_decode(layers, x, r, ws, ws_bytes, dev_status=None, stream=None):
+    """layers: a sequence of MoeqLayer (copied into one contiguous array)."""
+    arr = (MoeqLayer * len(layers))(*layers)
+    return _check("moe_ffn_stack_decode", load().moe_ffn_stack_decode(
+        arr, len(layers), _ptr(x), _ptr(r), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
 
 
 def moe_ffn_stack_prefill(layers, x, T, r, ws, ws_bytes, dev_status=None, stream=None):

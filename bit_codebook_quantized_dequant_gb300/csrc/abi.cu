@@ -78,6 +78,12 @@ using namespace moeq;
 
 extern "C" int moeq_packed_bytes(int fmt, int rows, int cols, size_t* code_bytes,
                                  size_t* scale_bytes) {
+  if (fmt == MOEQ_BF16) {  // unpacked rows
+    if (rows < 0 || cols < 0) return MOEQ_ERR_SHAPE;
+    if (code_bytes) *code_bytes = 2 * static_cast<size_t>(rows) * static_cast<size_t>(cols);
+    if (scale_bytes) *scale_bytes = 0;
+    return MOEQ_OK;
+  }
   if (fmt != 2 && fmt != 3 && fmt != 4) return MOEQ_ERR_FORMAT;
   if (rows < 0 || cols < 0 || cols % 32) return MOEQ_ERR_SHAPE;
   const size_t nblk = static_cast<size_t>(rows) * (cols / 32);
@@ -93,6 +99,9 @@ extern "C" size_t moe_ffn_workspace(const moeq_layer* L, int T_max, int mode) {
   if (mode == 0) return decode_ws_layout(L->H, L->I, L->E, L->k, L->has_shared).total;
   if (mode == 1) return verify_ws_layout(L->H, L->I, L->E, L->k, L->has_shared).total;
   if (mode == 2) return prefill_ws_layout(L->H, L->I, L->E, L->k, L->has_shared, T_max).total;
+  if (mode == 4)  // decode stack of layers shaped like L: decode workspace + a [H] bf16 + y [H] fp32
+    return decode_ws_layout(L->H, L->I, L->E, L->k, L->has_shared).total + align256(2 * static_cast<size_t>(L->H)) +
+           align256(4 * static_cast<size_t>(L->H));
   if (mode == 3)  // a stack of layers shaped like L: prefill workspace + the bf16 RMSNorm output
     return prefill_ws_layout(L->H, L->I, L->E, L->k, L->has_shared, T_max).total +
            align256(2 * static_cast<size_t>(T_max) * L->H);

@@ -1413,3 +1413,34 @@ extern "C" int moe_ffn_decode_static(const moeq_layer* L, const uint16_t* x, flo
   fill_args(a, L, 1, x, y, ws, wl, dev_status, nullptr);
   return launch<1>(a, false, stream);
 }
+
+extern "C" int moe_ffn_stack_decode(const moeq_layer* layers, int nlayers, const uint16_t* x, float* r,
+                                    void* ws, size_t ws_bytes, int32_t* dev_status, moeq_stream stream) {
+  if (!layers || nlayers < 1) return MOEQ_ERR_ARG;
+  const int H = layers[0].H;
+  size_t need = 0;
+  for (int l = 0; l < nlayers; ++l) {
+    const int rc = validate_layer(&layers[l]);
+    if (rc) return rc;
+    if (layers[l].H != H) return MOEQ_ERR_SHAPE;
+    if (!shapes_fit(&layers[l], 1)) return MOEQ_ERR_SHAPE;
+    const DecodeWs wl = decode_ws_layout(layers[l].H, layers[l].I, layers[l].E, layers[l].k,
+                                         layers[l].has_shared, 1);
+    need = wl.total > need ? wl.total : need;
+  }
+  if (!x || !r) return MOEQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(r)) return MOEQ_ERR_ALIGN;
+  const size_t abytes = align256(2 * static_cast<size_t>(H)), ybytes = align256(4 * static_cast<size_t>(H));
+  if (!ws || !aligned16(ws) || ws_bytes < need + abytes + ybytes) return MOEQ_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint16_t* a = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + need);
+  float* y = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + need + abytes);
+  // r_0 = float(x), a_0 = RMSNorm(r_0); per layer y = FFN_l(a_l), then
+  // r_{l+1} = r_l + y and a_{l+1} = RMSNorm(r_{l+1}) (no norm after the last)
+  int rc = stack_step_launch(x, nullptr, r, a, H, s);
+  for (int l = 0; l < nlayers && !rc; ++l) {
+    rc = moe_ffn_decode(&layers[l], a, y, ws, need, dev_status, nullptr, stream);
+    if (!rc) rc = stack_step_launch(nullptr, y, r, l + 1 < nlayers ? a : nullptr, H, s);
+  }
+  return rc;
+}

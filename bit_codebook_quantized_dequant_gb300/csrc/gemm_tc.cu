@@ -100,7 +100,13 @@ struct TcSmem {
   uint32_t nmma[kStages];             // MMA N of the stage (its tile's rows, rounded up to 16)
   uint32_t tmem_base;
   volatile int abort;
+  volatile int drained;               // every MMA of this CTA has completed
 };
+
+// Waits with no dependency on another CTA (MMA completion, landing of this
+// CTA's own copies) end unless the hardware is broken: they get a longer limit
+// than the ring waits, so that a ring timeout never cuts them short.
+constexpr uint32_t kDrainLimit = kSpinLimit * 16;
 static_assert(kAcol0 + kStages * 2 * 32 <= kTmemCols, "TMEM: accumulators + weight ring");
 
 enum EpiKind { EPI_G = 0, EPI_SWIGLU = 1, EPI_O = 2 };
@@ -395,6 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
+    sm.drained = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -555,7 +562,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     if (lane == 0) {
       for (int j = max(0, ks - kStages); j < ks; ++j) {
         bool done = false;
-        for (uint32_t i = 0; i < kSpinLimit && !done; ++i)
+        for (uint32_t i = 0; i < kDrainLimit && !done; ++i)
           done = mbar_try_wait_sleep(&sm.full_b[j % kStages], (j / kStages) & 1);
         if (!done) {
           set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
@@ -603,8 +610,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       // (also when a wait above ran out and the loops were left early)
       mma_commit(&sm.drain);
       bool drained = false;
-      for (uint32_t i = 0; i < kSpinLimit && !drained; ++i) drained = mbar_try_wait_sleep(&sm.drain, 0);
+      for (uint32_t i = 0; i < kDrainLimit && !drained; ++i) drained = mbar_try_wait_sleep(&sm.drain, 0);
       if (!drained) set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+      sm.drained = drained ? 1 : 0;
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
@@ -684,7 +692,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  // TMEM is released only once no MMA of this CTA can still write it; if the
+  // drain wait itself ran out (broken hardware, reported in the status), the
+  // CTA exits holding it rather than free columns under an MMA in flight
+  if (warp == kMmaWarp && sm.drained) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "n"(kTmemCols));
   }

@@ -84,6 +84,10 @@ struct TcGemm {
 };
 int tc_grouped_gemm(const TcGemm& g, cudaStream_t s);
 
+// One step of a decode stack on one token (route.cu): r = float(x) if x, else
+// r += y if y; then a = RMSNorm(r) if a. One warp.
+int stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, cudaStream_t s);
+
 // Router + top-k of T tokens enqueued on s (route.cu).
 int route_topk_launch(const uint16_t* x, int T, const uint16_t* router, int E, int H, int k,
                       int32_t* idx, float* w, float* logits, cudaStream_t s);

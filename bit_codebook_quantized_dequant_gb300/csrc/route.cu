@@ -123,13 +123,9 @@ __global__ void h32_kernel(const float* __restrict__ in, float* out, int nblk,
   out[static_cast<size_t>(b) * 32 + lane] = h32_warp(v, signs ? signs[b] : 0u, lane);
 }
 
-// One warp per row: sum of squares in the canonical order, correctly rounded
-// fp32 steps, then a = bf16_rne(r * inv).
-__global__ void rmsnorm_kernel(const float* __restrict__ r, int T, int H, uint16_t* __restrict__ a) {
-  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const float* row = r + static_cast<size_t>(t) * H;
+// RMSNorm of one row by one warp: sum of squares in the canonical order,
+// correctly rounded fp32 steps, then a = bf16_rne(r * inv).
+__device__ __forceinline__ void rmsnorm_row(const float* row, int H, uint16_t* out, int lane) {
   float s = 0.0f;
   for (int i = 0; i < H / 256; ++i) {
     const float4 v0 = *reinterpret_cast<const float4*>(row + 256 * i + 8 * lane);
@@ -146,7 +142,6 @@ __global__ void rmsnorm_kernel(const float* __restrict__ r, int T, int H, uint16
   s = warp_sum_canonical(s);
   const float ms = __fdiv_rn(s, static_cast<float>(H));
   const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, 1e-6f)));
-  uint16_t* out = a + static_cast<size_t>(t) * H;
   for (int k0 = 8 * lane; k0 < H; k0 += 256) {
     const float4 v0 = *reinterpret_cast<const float4*>(row + k0);
     const float4 v1 = *reinterpret_cast<const float4*>(row + k0 + 4);
@@ -157,6 +152,30 @@ __global__ void rmsnorm_kernel(const float* __restrict__ r, int T, int H, uint16
     o.w = f32_to_bf16_rne(__fmul_rn(v1.z, inv)) | (static_cast<uint32_t>(f32_to_bf16_rne(__fmul_rn(v1.w, inv))) << 16);
     *reinterpret_cast<uint4*>(out + k0) = o;
   }
+}
+
+__global__ void rmsnorm_kernel(const float* __restrict__ r, int T, int H, uint16_t* __restrict__ a) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  rmsnorm_row(r + static_cast<size_t>(t) * H, H, a + static_cast<size_t>(t) * H, lane);
+}
+
+// One step of a decode stack on one token (one warp): r = float(x) when x is
+// given, else r = r + y when y is given (correctly rounded fp32 adds); then,
+// when a is given, a = RMSNorm(r) as moe_rmsnorm_bf16.
+__global__ void stack_step_kernel(const uint16_t* __restrict__ x, const float* __restrict__ y,
+                                  float* __restrict__ r, uint16_t* __restrict__ a, int H) {
+  const int lane = threadIdx.x & 31;
+  for (int k = lane; k < H; k += 32) {
+    if (x) {
+      r[k] = __uint_as_float(static_cast<uint32_t>(x[k]) << 16);
+    } else if (y) {
+      r[k] = __fadd_rn(r[k], y[k]);
+    }
+  }
+  __syncwarp();
+  if (a) rmsnorm_row(r, H, a, lane);
 }
 
 }  // namespace
@@ -200,6 +219,12 @@ extern "C" int h32_rotate(const float* in, float* out, int nblk, const uint32_t*
   const int per = 8;  // blocks per CTA
   h32_kernel<<<(nblk + per - 1) / per, per * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       in, out, nblk, signs);
+  return cuda_status(cudaGetLastError());
+}
+
+// Enqueues one stack step (see stack_step_kernel).
+int moeq::stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, cudaStream_t s) {
+  stack_step_kernel<<<1, 32, 0, s>>>(x, y, r, a, H);
   return cuda_status(cudaGetLastError());
 }
 

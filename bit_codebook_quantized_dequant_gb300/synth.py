@@ -194,12 +194,18 @@ WORKLOADS = {
             h32=False, T=1, layers=1, dense=False),
     "verify-q4": dict(name="verify-q4", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3, shared_fmt=4,
             h32=False, T=4, layers=1, dense=True),
+    # format variants of the decode layer: top-4 routing, and FP2 down projections
+    "decode-b1-top4": dict(name="decode-b1-top4", H=4096, I=2048, E=256, k=4, fmt_gu=2, fmt_down=3,
+            shared_fmt=4, h32=False, T=1, layers=1, dense=False),
+    "decode-b1-fp2down": dict(name="decode-b1-fp2down", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=2,
+            shared_fmt=4, h32=False, T=1, layers=1, dense=False),
     "prefill-h32-fp4": dict(name="prefill-h32-fp4", H=4096, I=2048, E=256, k=6, fmt_gu=4, fmt_down=4,
             shared_fmt=None, h32=True, T=2048, layers=1, dense=False),
     "prefill-43-layer-stack": dict(name="prefill-43-layer-stack", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3,
             shared_fmt=4, h32=False, T=32512, layers=43, dense=False),
 }
-WORKLOAD_ORDER = ("tiny-decode", "decode-b1", "verify-q4", "prefill-h32-fp4", "prefill-43-layer-stack")
+WORKLOAD_ORDER = ("tiny-decode", "decode-b1", "verify-q4", "prefill-h32-fp4", "prefill-43-layer-stack",
+                  "decode-b1-top4", "decode-b1-fp2down")
 
 # (role, rows-is-I?) for the matrices of a layer: gate/up are [I x H], down [H x I]
 MATRIX_ROLES = {
@@ -265,6 +271,37 @@ def tokens(seed, cfg, count, start=0, layer=0):
     u2 = (ub >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
     z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
     return f32_to_bf16_bits(z.astype(np.float32)).reshape(count, H)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def selection_gap(seed, cfg, token=0, layer=0) -> float:
+    """Workload screening: the absolute gap between the k-th and (k+1)-th
+    largest router logits of one token, from the bf16 inputs in fp64 (a plain
+    dot product; the decision itself is taken in the kernels' fp32 order)."""
+    x = bf16_bits_to_f64(tokens(seed, cfg, 1, start=token, layer=layer)[0])
+    w = bf16_bits_to_f64(router_weights(seed, layer, cfg))
+    lg = np.sort(w @ x)[::-1]
+    k = cfg["k"]
+    return float(lg[k - 1] - lg[k])
+
+
+CONFIG0_MIN_GAP = 1e-3
+
+
+def config0_seeds(count: int, cfg=None, min_gap: float = CONFIG0_MIN_GAP):
+    """Seeds of the tiny decode workload (one token each, token 0 of layer 0):
+    consecutive seeds from the workload's base seed, skipping those whose
+    rank-k / rank-(k+1) router logit gap is below min_gap."""
+    cfg = cfg or WORKLOADS["tiny-decode"]
+    out, s = [], workload_seed("tiny-decode")
+    while len(out) < count:
+        if selection_gap(s, cfg) >= min_gap:
+            out.append(s)
+        s += 1
+    return out
 
 
 def h32_signs(seed, layer, cfg, which):

@@ -43,7 +43,11 @@ extern "C" {
 
 typedef struct CUstream_st* moeq_stream; /* a cudaStream_t; NULL = legacy default stream */
 
-typedef enum { MOEQ_FP2 = 2, MOEQ_FP3 = 3, MOEQ_FP4 = 4 } moeq_fmt;
+/* Weight formats. FP2/FP3/FP4: packed 32-weight codebook blocks (the layer
+ * roles). MOEQ_BF16: unpacked bf16 rows, no scales or codebooks (the router's
+ * format; no packed role takes it, moeq_packed_bytes sizes it as rows x cols
+ * x 2 bytes of codes and no scale plane). */
+typedef enum { MOEQ_FP2 = 2, MOEQ_FP3 = 3, MOEQ_FP4 = 4, MOEQ_BF16 = 16 } moeq_fmt;
 
 typedef enum {
   MOEQ_OK = 0,
@@ -131,7 +135,9 @@ enum {
 
 /* ---------------------------------------------------------------- sizes */
 
-/* Bytes of the two planes of one packed matrix. Returns MOEQ_OK or an error. */
+/* Bytes of the two planes of one matrix of format fmt (for MOEQ_BF16 the
+ * code plane is the bf16 rows and the scale plane is empty). Returns MOEQ_OK
+ * or an error. */
 int moeq_packed_bytes(int fmt, int rows, int cols, size_t* code_bytes, size_t* scale_bytes);
 
 /* Host-side checks of a layer descriptor (shapes, formats, alignment,
@@ -143,7 +149,8 @@ int moeq_validate_layer(const moeq_layer* L);
 
 /* Workspace bytes for a call: mode 0 = decode, 1 = q=4 verify, 2 = prefill of
  * up to T_max tokens, 3 = moe_ffn_stack_prefill of up to T_max tokens through
- * layers shaped like L. 0 on an invalid descriptor. */
+ * layers shaped like L, 4 = moe_ffn_stack_decode through layers shaped like L
+ * (T_max is ignored for modes 0, 1 and 4). 0 on an invalid descriptor. */
 size_t moe_ffn_workspace(const moeq_layer* L, int T_max, int mode);
 
 /* Zero a freshly allocated workspace (enqueued memset). Needed once; every
@@ -152,13 +159,48 @@ int moe_ffn_workspace_init(void* ws, size_t ws_bytes, moeq_stream stream);
 
 /* ---------------------------------------------------------------- entry points */
 
-/* Pack one matrix: codes_u8 [rows x cols] (one code per byte, < 2^fmt) and
- * scales [rows x cols/32] (fp16 bits or E8M0 bytes, row-major) into the code
- * plane out_codes and the scale plane out_scales (the scale plane has the
- * input's layout; it is copied). A code out of range sets *dev_status to
- * MOEQ_ERR_DEVICE_INDEX and is packed masked to fmt bits. */
+/* Pack one matrix into the block formats of "DeepSeek V4 Flash: 284B model,
+ * up to 32 tok/s on AMD Ryzen AI MAX+ 395", section "ROCmFPX: fitting 284B
+ * weights into 128 GB" (blocks of 32 weights stored as small codebook codes
+ * with one small scale each; FP2 2.5, FP3 3.5, FP4 4.25 bits per weight):
+ * codes_u8 [rows x cols] (one code per byte, < 2^fmt) and scales
+ * [rows x cols/32] (fp16 bits for FP2/FP3, E8M0 bytes for FP4, row-major) go
+ * to the code plane out_codes (per 32-block: FP2 8 bytes of 2-bit codes, FP3
+ * 12 bytes: the low two bits of the codes in two words and their third bits in
+ * a third, FP4 16 bytes of nibbles)
+ * and the scale plane out_scales (the input's layout; it is copied). fmt is 2,
+ * 3 or 4 (MOEQ_ERR_FORMAT otherwise); cols % 32 == 0; all pointers are device
+ * pointers owned by the caller, 16-byte aligned. A code out of range sets
+ * *dev_status to MOEQ_ERR_DEVICE_INDEX and is packed masked to fmt bits. */
 int moe_pack_expert(int fmt, int rows, int cols, const uint8_t* codes_u8, const void* scales,
                     void* out_codes, void* out_scales, int32_t* dev_status, moeq_stream stream);
+
+/* Codebook quantization of one expert matrix: fp32 weights -> the inputs of
+ * moe_pack_expert (codes, block scales) and the expert's codebook. The pages
+ * name "learned per-expert codebooks" ("Lucebox x Geometric ...", section
+ * "How the model fits on AMD Strix Halo") without printing how they are
+ * learned; this is the library's reading, deterministic and exact in its
+ * integer steps:
+ *   1. per 32-block, m = max |w|: FP2/FP3 scale d = fp16_rne(m / 127) (fp32
+ *      division; the largest finite fp16 on overflow); FP4 E8M0 byte e + 127
+ *      with e the smallest integer >= -127 such that 127 * 2^e >= m (<= 127);
+ *   2. v = w / d (fp32; 0 where d == 0), g = clamp(rint(v), -127, 127), and
+ *      the histogram of g over the whole matrix;
+ *   3. 2^fmt int8 entries start at the histogram's mid-quantiles (entry i =
+ *      the smallest g whose cumulative count exceeds floor((2i+1)N / 2^(fmt+1)),
+ *      N weights), then 8 Lloyd steps on the histogram in integers (each g to
+ *      its nearest entry, ties to the lower index; each entry with a non-empty
+ *      cell to the cell's mean rounded half up; entries sorted ascending);
+ *   4. each weight's code = the entry nearest to v in fp32, ties to the lower
+ *      index.
+ * w [rows x cols] fp32 (16-byte aligned), codes_u8 [rows x cols], scales
+ * [rows x cols/32] (fp16 bits for FP2/FP3, E8M0 bytes for FP4), codebook
+ * [2^fmt] int8; all device memory owned by the caller. ws: >= 1 KiB of device
+ * memory (16-byte aligned), cleared by the call. cols % 32 == 0,
+ * rows * cols < 2^31. Three kernels enqueued on the stream. */
+int moe_quantize_expert(int fmt, int rows, int cols, const float* w, uint8_t* codes_u8, void* scales,
+                        int8_t* codebook, void* ws, size_t ws_bytes, int32_t* dev_status,
+                        moeq_stream stream);
 
 /* Router and top-k for T tokens ("DeepSeek V4 Flash: 284B model ...", section
  * "Decode: up to 32 tok/s": routing with dedicated TOP_K kernels):
@@ -258,6 +300,20 @@ int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, const float* 
  * the stream, no host synchronization. */
 int moe_ffn_stack_prefill(const moeq_layer* layers, int nlayers, const uint16_t* x, int T, float* r,
                           void* ws, size_t ws_bytes, int32_t* dev_status, moeq_stream stream);
+
+/* One decode token through a stack of nlayers layers (layers[l], all with the
+ * same H) with an fp32 residual stream ("DeepSeek V4 Flash: 284B model ...",
+ * section "ROCmFPX: fitting 284B weights into 128 GB": every generated token
+ * streams the active weights of every layer):
+ *   r_0 = float(x);  a_l = moe_rmsnorm_bf16(r_l);  r_{l+1} = r_l + y_l
+ * with y_l = moe_ffn_decode of layer l on a_l and correctly rounded fp32 adds.
+ * x [H] bf16; r [H] fp32 receives r_nlayers. ws: at least
+ * moe_ffn_workspace(L, 1, 4) bytes for the largest layer shape, zeroed once
+ * with moe_ffn_workspace_init (its decode part is reused by every layer in
+ * turn). 2 * nlayers + 1 kernels enqueued on the stream, no host
+ * synchronization; the shapes each decode takes are those of moe_ffn_decode. */
+int moe_ffn_stack_decode(const moeq_layer* layers, int nlayers, const uint16_t* x, float* r,
+                         void* ws, size_t ws_bytes, int32_t* dev_status, moeq_stream stream);
 
 /* H32 rotation ("deepseek-v4-flash-0731-evox3-rocm", section "The optimization
  * ladder"): out = H D in per 32-block, H the 32x32 Sylvester Hadamard matrix

@@ -98,6 +98,7 @@ def _declare(L):
     L.orc_ffn_prefill.argtypes = [C.POINTER(OrcLayer), P, C.c_int, P]
     L.orc_rmsnorm_bf16.argtypes = [P, C.c_int, P]
     L.orc_rmsnorm_bf16.restype = None
+    L.orc_quantize_expert.argtypes = [C.c_int, C.c_int, C.c_int, P, P, P, P]
 
 
 def _p(a: Optional[np.ndarray]):
@@ -343,3 +344,16 @@ def ffn_prefill(L: Layer, x_bf16: np.ndarray):
     y = np.zeros((T, L.H), dtype=np.float64)
     _chk(lib().orc_ffn_prefill(C.byref(cl), _p(x), T, _p(y)), "ffn_prefill")
     return y
+
+
+def quantize_expert(fmt: int, w: np.ndarray):
+    """Codebook quantization of one expert matrix (fp32 [rows, cols]) -> codes
+    (uint8 [rows, cols]), scales (fp16 bits uint16 or E8M0 uint8 [rows, cols/32])
+    and the codebook (int8 [2^fmt]); see orc_quantize_expert."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    codes = np.zeros((rows, cols), np.uint8)
+    scales = np.zeros((rows, cols // 32), np.uint8 if fmt == 4 else np.uint16)
+    cb = np.zeros(1 << fmt, np.int8)
+    _chk(lib().orc_quantize_expert(fmt, rows, cols, _p(w), _p(codes), _p(scales), _p(cb)), "quantize_expert")
+    return codes, scales, cb

@@ -516,3 +516,120 @@ void orc_rmsnorm_bf16(const float* r, int H, uint16_t* a) {
     a[k] = orc_f32_to_bf16(v);
   }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Codebook quantization of one expert matrix w [rows x cols] fp32 into the  */
+/* block formats ("Lucebox x Geometric ...", section "How the model fits on */
+/* AMD Strix Halo": learned per-expert codebooks; how they are learned is    */
+/* not printed, so this is the library's reading, plain and deterministic):  */
+/*  1. block scale d per 32-block, m = max |w| of the block:                 */
+/*     FP2/FP3: d = fp16_rne(m / 127) (fp32 division, RN; the Q8 rule),      */
+/*              the largest finite fp16 if that overflows;                   */
+/*     FP4: E8M0 byte b = e + 127, e the smallest integer with               */
+/*          127 * 2^e >= m, clamped to [-127, 127] (m = 0 gives e = -127).   */
+/*  2. v = w / d in fp32 (RN); v = 0 where d == 0.                            */
+/*  3. histogram of g = clamp(rint(v), -127, 127) over the whole matrix.      */
+/*  4. K = 2^fmt int8 entries: entry i starts at the smallest g whose        */
+/*     cumulative count exceeds floor((2i+1) N / (2K)) (N weights); then 8    */
+/*     Lloyd steps on the histogram, exact in integers: each grid value goes  */
+/*     to its nearest entry (ties to the lower index), each entry with a     */
+/*     non-empty cell becomes floor((2 S + n) / (2 n)) (S the cell's sum of  */
+/*     g, n its count: the mean rounded half up), then the entries are       */
+/*     sorted ascending.                                                     */
+/*  5. code of each weight = the entry nearest to v, |v - c| in fp32, ties   */
+/*     to the lower index.                                                   */
+/* Outputs: codes [rows x cols] one per byte, scales [rows x cols/32] (fp16  */
+/* bits or E8M0 bytes), cb [2^fmt].                                          */
+/* ------------------------------------------------------------------------ */
+static int64_t floor_div64(int64_t a, int64_t b) { /* b > 0 */
+  int64_t q = a / b;
+  if ((a % b) != 0 && a < 0) q -= 1;
+  return q;
+}
+
+static float block_scale_q(int fmt, const float* blk, void* scales, size_t i) {
+  float m = 0.0f;
+  for (int j = 0; j < 32; j++) {
+    float a = fabsf(blk[j]);
+    if (a > m) m = a;
+  }
+  if (fmt == 4) {
+    int e = -127;
+    while (e < 127 && ldexp(127.0, e) < (double)m) e++;
+    ((uint8_t*)scales)[i] = (uint8_t)(e + 127);
+    return (float)ldexp(1.0, e);
+  }
+  volatile float dq = m / 127.0f;
+  uint16_t dh = orc_f32_to_f16(dq);
+  if ((dh & 0x7C00u) == 0x7C00u) dh = 0x7BFFu; /* overflow: the largest finite fp16 */
+  ((uint16_t*)scales)[i] = dh;
+  return (float)orc_f16_to_f64(dh);
+}
+
+int orc_quantize_expert(int fmt, int rows, int cols, const float* w, uint8_t* codes, void* scales,
+                        int8_t* cb) {
+  if (fmt < 2 || fmt > 4) return ORC_ERR_ARG;
+  if (rows <= 0 || cols <= 0 || cols % 32) return ORC_ERR_ARG;
+  const int K = 1 << fmt, nb = cols / 32;
+  int64_t hist[255] = {0};
+  const size_t N = (size_t)rows * cols;
+  float* v = (float*)malloc(N * sizeof(float));
+  if (!v) return ORC_ERR_ARG;
+  for (int r = 0; r < rows; r++)
+    for (int b = 0; b < nb; b++) {
+      const size_t o = (size_t)r * cols + 32 * b;
+      const float d = block_scale_q(fmt, w + o, scales, (size_t)r * nb + b);
+      for (int j = 0; j < 32; j++) {
+        volatile float t = d == 0.0f ? 0.0f : w[o + j] / d;
+        v[o + j] = t;
+        float g = rintf(t);
+        if (g > 127.0f) g = 127.0f;
+        if (g < -127.0f) g = -127.0f;
+        hist[(int)g + 127]++;
+      }
+    }
+  int64_t c[16];
+  for (int i = 0; i < K; i++) {
+    const int64_t t = ((2 * (int64_t)i + 1) * (int64_t)N) / (2 * (int64_t)K);
+    int64_t cum = 0;
+    int g = 0;
+    for (; g < 255; g++) {
+      cum += hist[g];
+      if (cum > t) break;
+    }
+    c[i] = g - 127;
+  }
+  for (int it = 0; it < 8; it++) {
+    int64_t S[16] = {0}, n[16] = {0};
+    for (int g = 0; g < 255; g++) {
+      if (!hist[g]) continue;
+      const int64_t x = g - 127;
+      int best = 0;
+      int64_t bd = llabs(x - c[0]);
+      for (int i = 1; i < K; i++) {
+        const int64_t dd = llabs(x - c[i]);
+        if (dd < bd) { bd = dd; best = i; }
+      }
+      S[best] += hist[g] * x;
+      n[best] += hist[g];
+    }
+    for (int i = 0; i < K; i++)
+      if (n[i]) c[i] = floor_div64(2 * S[i] + n[i], 2 * n[i]);
+    for (int i = 1; i < K; i++) /* insertion sort, ascending */
+      for (int j = i; j > 0 && c[j - 1] > c[j]; j--) {
+        int64_t tmp = c[j]; c[j] = c[j - 1]; c[j - 1] = tmp;
+      }
+  }
+  for (int i = 0; i < K; i++) cb[i] = (int8_t)c[i];
+  for (size_t o = 0; o < N; o++) {
+    int best = 0;
+    float bd = fabsf(v[o] - (float)c[0]);
+    for (int i = 1; i < K; i++) {
+      const float dd = fabsf(v[o] - (float)c[i]);
+      if (dd < bd) { bd = dd; best = i; }
+    }
+    codes[o] = (uint8_t)best;
+  }
+  free(v);
+  return ORC_OK;
+}

@@ -119,6 +119,8 @@ int orc_ffn_prefill(const orc_layer* L, const uint16_t* x, int T, double* y);
 
 /* layer stack helpers */
 void orc_rmsnorm_bf16(const float* r, int H, uint16_t* a);
+int orc_quantize_expert(int fmt, int rows, int cols, const float* w, uint8_t* codes, void* scales,
+                        int8_t* cb);
 
 #ifdef __cplusplus
 }

@@ -52,6 +52,42 @@ def output_bound(L: O.Layer, idx, p, hq, hd) -> np.ndarray:
     return sum(wi * bi for wi, bi in zip(w, b))
 
 
+def requant_bound(L: O.Layer, idx, p, hq_a, hd_a, hq_b, hd_b) -> np.ndarray:
+    """D_r = sum_slot p_slot sum_k |w_down[r,k]| |h~a_k - h~b_k|: how far the
+    down projection and combine of two quantized h (the GPU's and the oracle's
+    own) can move y apart, in exact arithmetic."""
+    slots = [(L.down, int(e)) for e in idx]
+    if L.shared is not None:
+        slots.append((L.shared[2], 0))
+    w = list(p) + ([1.0] if L.shared is not None else [])
+    D = np.zeros(L.H)
+    for s, (m, e) in enumerate(slots):
+        ta = hq_a[s].astype(np.float64) * np.repeat(O.f16_array_to_f64(hd_a[s]), 32)
+        tb = hq_b[s].astype(np.float64) * np.repeat(O.f16_array_to_f64(hd_b[s]), 32)
+        dh = np.abs(ta - tb)
+        nz = np.nonzero(dh)[0]
+        if nz.size:  # only the columns where the two differ
+            codes = O.unpack(m.fmt, m.rows, m.cols, m.codes[e])[:, nz]
+            sv = O.scale_values(m.fmt, m.scales[e]).reshape(m.rows, m.cols // 32)[:, nz // 32]
+            D += w[s] * (np.abs(sv * m.cb[e].astype(np.float64)[codes]) @ dh[nz])
+    return D
+
+
+def check_independent(y_gpu, y_ora, bound, requant, what=""):
+    """y against the independent fp64 oracle: the teacher-forced bound widened
+    by requant_bound (the part of the difference that comes from the two sides
+    quantizing their own h)."""
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    err = np.abs(y_gpu - y_ora)
+    lim = ELEM * bound + requant
+    worst = np.max(err / np.maximum(lim, 1e-300))
+    rel = np.linalg.norm(y_gpu - y_ora) / max(np.linalg.norm(y_ora), 1e-300)
+    rel_lim = REL_L2 + np.linalg.norm(requant) / max(np.linalg.norm(y_ora), 1e-300)
+    assert np.all(err <= lim), f"{what}: max |err| / (2e-3 B + D) = {worst:.3g} > 1"
+    assert rel <= rel_lim, f"{what}: relative L2 {rel:.3g} > {rel_lim:.3g}"
+    return worst, rel
+
+
 def check_output(y_gpu, y_ref, bound, what=""):
     y_gpu = np.asarray(y_gpu, dtype=np.float64)
     err = np.abs(y_gpu - y_ref)
@@ -130,6 +166,9 @@ def check_token(L, cfg, x_row, y, g, partials, flip_frac=FLIPS_DECODE, h_atol=H_
         assert np.all(err <= o_rel * bs), f"o[{s}]: max err/bound {np.max(err / bs):.3g}"
     check_output(y, yt, B, "y (teacher-forced)")
     same_q = np.array_equal(hq, tr["hq"][:ns]) and np.array_equal(hd, tr["hd"][:ns])
+    # and against the independent oracle output
+    D = requant_bound(L, tr["idx"], tr["p"], hq, hd, tr["hq"][:ns], tr["hd"][:ns])
+    check_independent(y, yo, B, D, "y (independent)")
     return yo, B, same_q
 
 

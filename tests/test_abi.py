@@ -36,8 +36,12 @@ def test_packed_bytes():
     assert M.moeq_packed_bytes(2, 2048, 4096) == (2048 * 128 * 8, 2048 * 128 * 2)
     assert M.moeq_packed_bytes(3, 4096, 2048) == (4096 * 64 * 12, 4096 * 64 * 2)
     assert M.moeq_packed_bytes(4, 2048, 4096) == (2048 * 128 * 16, 2048 * 128)
+    # unpacked bf16 rows: two bytes per weight, no scale plane
+    assert M.moeq_packed_bytes(M.MOEQ_BF16, 256, 4096) == (256 * 4096 * 2, 0)
     with pytest.raises(M.MoeqError):
         M.moeq_packed_bytes(5, 1, 32)
+    # no packed role takes MOEQ_BF16
+    assert M.moeq_validate_layer(_layer(gate=_mat(M.MOEQ_BF16, 256, 256, 16))) == M.CODE["MOEQ_ERR_FORMAT"]
 
 
 FAKE = 1 << 40  # aligned fake device address: validation never dereferences
@@ -129,6 +133,14 @@ def test_entry_points_reject_bad_arguments_before_launch():
     assert lib.moe_ffn_decode_static(C.byref(big), FAKE, FAKE, None, None) == \
         M.CODE["MOEQ_ERR_WORKSPACE"]
     assert lib.moe_ffn_decode_static(C.byref(L), None, FAKE, None, None) == M.CODE["MOEQ_ERR_ARG"]
+    # decode stack: layers, then the workspace (decode + a + y for the largest layer)
+    assert lib.moe_ffn_stack_decode(None, 1, FAKE, FAKE, FAKE, 1 << 30, None, None) == M.CODE["MOEQ_ERR_ARG"]
+    arr = (M.MoeqLayer * 2)(L, L)
+    need_s = lib.moe_ffn_workspace(C.byref(L), 1, 4)
+    assert need_s > need1
+    assert lib.moe_ffn_stack_decode(arr, 2, FAKE, FAKE, FAKE, need_s - 16, None, None) == \
+        M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert lib.moe_ffn_stack_decode(arr, 2, FAKE + 8, FAKE, FAKE, need_s, None, None) == M.CODE["MOEQ_ERR_ALIGN"]
     assert lib.h32_rotate(None, None, 4, None, None) == M.CODE["MOEQ_ERR_ARG"]
     assert lib.moe_rmsnorm_bf16(FAKE, 1, 100, FAKE, None) == M.CODE["MOEQ_ERR_SHAPE"]
 

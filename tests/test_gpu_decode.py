@@ -11,7 +11,7 @@ import bit_codebook_quantized_dequant_gb300 as M
 from bit_codebook_quantized_dequant_gb300 import synth as S
 from bit_codebook_quantized_dequant_gb300.workload import (Debug, Workspace, build_layer,
                                                            to_dev_u16)
-from _parity import check_output, check_token, host_layer_for
+from _parity import check_token, host_layer_for
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +43,16 @@ def test_decode_tiny(variant):
     elif variant == "cfg0-fp2-down":
         over = dict(fmt_down=2, shared_fmt=4)
     cfg = _cfg("tiny-decode", **over)
+    if variant == "cfg0":
+        # the tiny workload as stated: one token per seed, seeds whose rank-2/3
+        # router logit gap is below 1e-3 rejected
+        for seed in S.config0_seeds(48, cfg):
+            dl = build_layer(seed, 0, cfg)
+            x = S.tokens(seed, cfg, 1)
+            L = host_layer_for(seed, 0, cfg, x)
+            y, g = _run(dl, Workspace(dl, 0), x[0], partials=True)
+            check_token(L, cfg, x[0], y, g, partials=True)
+        return
     seed = S.workload_seed("tiny-decode") + 17 * len(variant)
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 0)
@@ -50,9 +60,7 @@ def test_decode_tiny(variant):
     L = host_layer_for(seed, 0, cfg, xs)
     for t in range(xs.shape[0]):
         y, g = _run(dl, ws, xs[t], partials=True)
-        yo, B, same_q = check_token(L, cfg, xs[t], y, g, partials=True)
-        if same_q:  # no fp32-vs-fp64 rounding of h crossed a quantization step
-            check_output(y, yo, B, "y (independent)")
+        check_token(L, cfg, xs[t], y, g, partials=True)
 
 
 def test_decode_config1_sampled_tokens():
@@ -60,7 +68,21 @@ def test_decode_config1_sampled_tokens():
     seed = S.workload_seed("decode-b1")
     dl = build_layer(seed, 0, cfg)
     ws = Workspace(dl, 0)
-    xs = S.tokens(seed, cfg, 3, start=0)
+    xs = S.tokens(seed, cfg, 64, start=0)
+    L = host_layer_for(seed, 0, cfg, xs)
+    for t in range(xs.shape[0]):
+        y, g = _run(dl, ws, xs[t], partials=(t == 0))
+        check_token(L, cfg, xs[t], y, g, partials=(t == 0))
+
+
+@pytest.mark.parametrize("name", ["decode-b1-top4", "decode-b1-fp2down"])
+def test_decode_format_variants(name):
+    # top-4 routing, and FP2 down projections, on the decode layer's shape
+    cfg = _cfg(name)
+    seed = S.workload_seed(name)
+    dl = build_layer(seed, 0, cfg)
+    ws = Workspace(dl, 0)
+    xs = S.tokens(seed, cfg, 8)
     L = host_layer_for(seed, 0, cfg, xs)
     for t in range(xs.shape[0]):
         y, g = _run(dl, ws, xs[t], partials=(t == 0))

@@ -68,7 +68,7 @@ def test_prefill_config3_sampled_tokens():
     dl = build_layer(seed, 0, cfg)
     T = 256
     X = S.tokens(seed, cfg, T)
-    _check_tokens(dl, seed, cfg, X, [0, 77, 255])
+    _check_tokens(dl, seed, cfg, X, list(range(0, T, 16)) + [T - 1])  # 17 tokens
 
 
 def test_prefill_matches_decode_and_residual():

@@ -2,7 +2,7 @@
 launch configuration bench.py times (one call of T tokens on the current
 stream): T = 2048 with FP4 experts and H32 on x and h, and T = 32512 on a
 layer of the 43-layer stack (FP2/FP3 routed experts, FP4 shared expert). On
-sampled tokens (first, second, middle, last) the same stage-by-stage checks
+sampled tokens (first, second, last and 13 spread over the rest) the same stage-by-stage checks
 as the smaller prefill tests: bit-exact xq/xd, logits and indices; h, hq/hd,
 the per-slot outputs and y against the oracle."""
 import numpy as np
@@ -53,7 +53,8 @@ def test_prefill_full_size_sampled_tokens(name, T):
     H = cfg["H"]
     dl = build_layer(seed, 0, cfg)
     X = S.tokens(seed, cfg, T)
-    sample = [0, 1, T // 2 + 3, T - 1]
+    # first, second, last and 13 tokens spread over the rest (16 in all)
+    sample = sorted({0, 1, T - 1} | {(T * j) // 14 + 3 for j in range(1, 14)})
     ws = Workspace(dl, 2, T)
     d = Debug(cfg, T)
     y = torch.zeros(T * H, dtype=torch.float32, device="cuda")

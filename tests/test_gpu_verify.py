@@ -52,26 +52,36 @@ def _decode(dl, ws1, x_row):
     return y.cpu().numpy()
 
 
-def _dense_bound(Dm: O.Matrix, xq, xd):
+def _abs_weights(Dm: O.Matrix):
     codes = O.unpack(Dm.fmt, Dm.rows, Dm.cols, Dm.codes[0])
     sv = O.scale_values(Dm.fmt, Dm.scales[0]).reshape(Dm.rows, Dm.cols // 32)
-    w = np.abs(np.repeat(sv, 32, axis=1) * Dm.cb[0].astype(np.float64)[codes])
+    return np.abs(np.repeat(sv, 32, axis=1) * Dm.cb[0].astype(np.float64)[codes])
+
+
+def _dense_bound(Wabs, xq, xd):
     xt = np.abs(xq.astype(np.float64) * np.repeat(O.f16_array_to_f64(xd), 32))
-    return w @ xt
+    return Wabs @ xt
 
 
-def _check_batch(dl, seed, cfg, X, partials, ws, ws1):
+def _check_batch(dl, seed, cfg, X, partials, ws, ws1, L=None, dense=None):
+    """One q=4 call on the 4 columns of X, checked column by column (L: an
+    oracle layer holding the columns' experts; dense: (matrix, |W|) of the
+    dense projection, built when not given)."""
     y, yd, g = _verify(dl, ws, X, partials)
-    L = host_layer_for(seed, 0, cfg, X)
+    if L is None:
+        L = host_layer_for(seed, 0, cfg, X)
     for c in range(4):
         check_token(L, cfg, X[c], y[c], column_view(g, cfg, c), partials)
         np.testing.assert_array_equal(y[c], _decode(dl, ws1, X[c]), err_msg=f"column {c}")
     if cfg["dense"]:
-        Dm = W.dense(seed, 0, cfg)
+        if dense is None:
+            Dm = W.dense(seed, 0, cfg)
+            dense = (Dm, _abs_weights(Dm))
+        Dm, Wabs = dense
         _, yd_ref = O.ffn_verify_q4(L, Dm, X)
         H = cfg["H"]
         for c in range(4):
-            B = _dense_bound(Dm, g["xq"][c * H:(c + 1) * H], g["xd"][c * (H // 32):(c + 1) * (H // 32)])
+            B = _dense_bound(Wabs, g["xq"][c * H:(c + 1) * H], g["xd"][c * (H // 32):(c + 1) * (H // 32)])
             check_output(yd[c * Dm.rows:(c + 1) * Dm.rows], yd_ref[c], B, f"y_dense[{c}]")
     return y
 
@@ -103,10 +113,15 @@ def test_verify_config2_sampled_batches():
     seed = S.workload_seed("verify-q4")
     dl = build_layer(seed, 0, cfg)
     ws, ws1 = Workspace(dl, 1), Workspace(dl, 0)
-    xs = S.tokens(seed, cfg, 8)
-    _check_batch(dl, seed, cfg, xs[0:4], True, ws, ws1)
+    nb = 16  # batches of 4 independently routed columns
+    xs = S.tokens(seed, cfg, 4 * nb)
+    L = host_layer_for(seed, 0, cfg, xs)
+    Dm = W.dense(seed, 0, cfg)
+    dense = (Dm, _abs_weights(Dm))
+    for b in range(nb):
+        _check_batch(dl, seed, cfg, xs[4 * b:4 * b + 4], b == 0, ws, ws1, L, dense)
     # two columns equal: their experts are read once for both
-    _check_batch(dl, seed, cfg, np.ascontiguousarray(xs[[4, 5, 4, 6]]), False, ws, ws1)
+    _check_batch(dl, seed, cfg, np.ascontiguousarray(xs[[4, 5, 4, 6]]), False, ws, ws1, L, dense)
 
 
 def test_verify_without_dense_and_repeatable():

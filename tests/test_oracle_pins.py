@@ -377,6 +377,21 @@ def test_prefill_and_q4_are_per_token_decode():
 
 
 # ----------------------------------------------------------------- RMSNorm
+def test_rmsnorm_order_golden():
+    n = 0
+    for H, entries, expect in _golden_lines("rmsnorm_order.txt"):
+        r = np.zeros(int(H), np.float32)
+        for ent in entries.split():
+            k, v = ent.split(":")
+            r[int(k)] = np.float32(float(v))
+        a = O.rmsnorm_bf16(r)
+        for ent in expect.split():
+            k, hx = ent.split(":")
+            assert int(a[int(k)]) == int(hx, 16), (k, hex(int(a[int(k)])), hx)
+        n += 1
+    assert n == 1
+
+
 def test_rmsnorm_bf16():
     a = O.rmsnorm_bf16(np.ones(4096, np.float32))
     assert np.all(a == 0x3F80)                      # 1 / sqrt(1 + 1e-6) rounds to bf16 1.0
@@ -388,3 +403,80 @@ def test_rmsnorm_bf16():
         ref = r64 / np.sqrt(np.mean(r64 ** 2) + 1e-6)
         ulp = 2.0 ** (np.floor(np.log2(np.abs(ref) + 1e-300)) - 7)
         assert np.all(np.abs(a - ref) <= ulp * 0.5001 + 1e-5 * np.abs(ref))
+
+
+# ----------------------------------------------------------------- codebook quantizer
+def _recoverable(fmt, rows=64, cols=256, seed=3):
+    """Weights built from a known sorted codebook, codes and block scales, with
+    one entry of magnitude 127 in every block (so that max|w| = 127 d)."""
+    rng = np.random.default_rng(seed)
+    K = 1 << fmt
+    inner = np.sort(rng.choice(np.arange(-120, 121), K - 2, replace=False))
+    cb = np.concatenate([[-127], inner, [127]]).astype(np.int8)
+    codes = rng.integers(0, K, size=(rows, cols)).astype(np.uint8)
+    codes[:, ::32] = np.where(rng.random((rows, cols // 32)) < 0.5, 0, K - 1)
+    if fmt == 4:
+        e = rng.integers(-20, -5, size=(rows, cols // 32))
+        d = np.ldexp(1.0, e).astype(np.float32)
+        sc = (e + 127).astype(np.uint8)
+    else:
+        d = np.float16(rng.uniform(1e-4, 1e-2, size=(rows, cols // 32))).astype(np.float32)
+        sc = d.astype(np.float16).view(np.uint16)
+    w = cb.astype(np.float32)[codes] * np.repeat(d, 32, axis=1)
+    return w, cb, codes, sc
+
+
+@pytest.mark.parametrize("fmt", [2, 3, 4])
+def test_quantizer_recovers_a_known_codebook(fmt):
+    w, cb, codes, sc = _recoverable(fmt)
+    c2, s2, cb2 = O.quantize_expert(fmt, w)
+    np.testing.assert_array_equal(cb2, cb)
+    np.testing.assert_array_equal(s2, sc)
+    np.testing.assert_array_equal(c2, codes)
+
+
+@pytest.mark.parametrize("fmt", [2, 3, 4])
+def test_quantizer_scales_codes_against_numpy(fmt):
+    rng = np.random.default_rng(20 + fmt)
+    w = (rng.standard_normal((48, 512)) * 0.02).astype(np.float32)
+    w[3, 32:64] = 0.0  # an all-zero block
+    codes, sc, cb = O.quantize_expert(fmt, w)
+    m = np.abs(w).reshape(48, 16, 32).max(axis=2)
+    if fmt == 4:
+        e = sc.astype(np.int64) - 127
+        d = np.ldexp(1.0, e)
+        pos = m > 0
+        assert np.all(127.0 * d >= m)                                  # |v| <= 127
+        assert np.all((127.0 * d / 2 < m)[pos & (e > -127)])           # smallest such power
+        assert np.all(e[~pos] == -127)
+    else:
+        ref = (m.astype(np.float32) / np.float32(127.0)).astype(np.float16)   # numpy RNE
+        np.testing.assert_array_equal(sc, ref.view(np.uint16))
+        d = ref.astype(np.float64)
+    # codebook: 2^fmt sorted int8 entries
+    assert cb.size == 1 << fmt and np.all(np.diff(cb.astype(int)) >= 0)
+    # every code is the nearest entry to v = w / d in fp32, ties to the lower index
+    df = np.repeat(d.astype(np.float32), 32, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(df == 0, np.float32(0), w / df).astype(np.float32)
+    dist = np.abs(v[..., None] - cb.astype(np.float32)[None, None, :])
+    np.testing.assert_array_equal(codes, np.argmin(dist, axis=2))
+
+
+def test_quantizer_ties_go_to_the_lower_entry():
+    # codebook {-127, -1, 1, 127}; zeros sit exactly between -1 and 1
+    fmt, rows, cols = 2, 8, 256
+    K = 4
+    cb = np.array([-127, -1, 1, 127], np.int8)
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, K, size=(rows, cols)).astype(np.uint8)
+    codes[:, ::32] = 3
+    d = np.float32(2.0 ** -10)
+    w = cb.astype(np.float32)[codes] * d
+    zero = rng.random((rows, cols)) < 0.01
+    zero[:, ::32] = False
+    w[zero] = 0.0
+    c2, _, cb2 = O.quantize_expert(fmt, w)
+    np.testing.assert_array_equal(cb2, cb)
+    assert np.all(c2[zero] == 1)          # |0 - (-1)| == |0 - 1|: the lower index
+    np.testing.assert_array_equal(c2[~zero], codes[~zero])
