@@ -550,7 +550,9 @@ def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind, cpu=False):
                              "as bf16 part products on the tensor cores)",
               "algorithmic_flops_per_launch": fl}
     hbm = {"bound": "hbm", "achieved": hbm_gbs, "peak": hbm_peak, "unit": "GB/s",
-           "frac": hbm_gbs / hbm_peak, "traffic": None,
+           "frac": hbm_gbs / hbm_peak,
+           "traffic": _traffic(f"prefill {name} gemm", "bit_codebook_quantized_dequant_gb300/csrc/gemm_tc.cu"),
+           "traffic_scope": "DRAM bytes of the gate, up and down tensor-core launches of one call",
            "peak_source": f"{peak_kind} hbm_gbs",
            "algorithmic_bytes_per_launch": wbytes}
     # the layer's bound: its FLOP per weight byte against the bf16 ridge
@@ -686,6 +688,67 @@ def bench_stack_decode(args, layers, cfg, seed):
                                       "oracle parity is a GPU test"}}
 
 
+def bench_expanded(args, hbm_peak, peak_kind):
+    """The expand-then-multiply ablation: one decode layer expanded to bf16
+    (12.9 GB), decoded with moe_ffn_decode_expanded, beside the fused decode
+    of the same packed layer on the same tokens; both from CUDA graphs."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, expand_layer, to_dev_u16
+    cfg = S.WORKLOADS[DECODE_WORKLOAD]
+    seed = S.workload_seed(DECODE_WORKLOAD)
+    dl = build_layer(seed, 7, cfg)
+    Lx, keep = expand_layer(dl)
+    H, I, k = cfg["H"], cfg["I"], cfg["k"]
+    ntok = 256
+    xs = to_dev_u16(S.tokens(seed, cfg, ntok, start=2048))
+    y = torch.zeros(H, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wsx_b = M.moe_ffn_expanded_workspace(H, I, k, 1)
+    wsx = torch.zeros(wsx_b, dtype=torch.uint8, device="cuda")
+    ws = Workspace(dl, 0)
+    desc = dl.desc()
+    stream = torch.cuda.Stream()
+
+    def fused(i, s):
+        M.moe_ffn_decode(desc, xs.data_ptr() + (i % ntok) * H * 2, y, ws.ptr, ws.nbytes, st, None, s)
+
+    def expanded(i, s):
+        M.moe_ffn_decode_expanded(Lx, xs.data_ptr() + (i % ntok) * H * 2, y, wsx, wsx_b, st, s)
+
+    out = {}
+    steps = 128
+    for name, fn in (("fused", fused), ("expanded", expanded)):
+        for i in range(5):
+            fn(i, stream)
+        torch.cuda.synchronize()
+        graphs = capture_steps(fn, 5, steps, stream)
+        replay(graphs, stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay(graphs, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / steps
+        del graphs
+    assert st.item() == 0, f"device status {st.item()}"
+    ns = k + 1
+    xbytes = 2 * (2 * ns * I * H + ns * H * I) + cfg["E"] * H * 2
+    res = {"metric": "expand-then-multiply ablation: decode us/token, fused vs expanded bf16 GEMV",
+           "us_fused": out["fused"] * 1e3, "us_expanded": out["expanded"] * 1e3,
+           "fused_speedup": out["expanded"] / out["fused"],
+           "bytes_fused": algorithmic_bytes_decode(cfg), "bytes_expanded": xbytes,
+           "expanded_hbm_frac": xbytes / (out["expanded"] * 1e-3) / 1e9 / hbm_peak,
+           "workload": "one decode-b1 layer (replica 7), 1 layer resident packed (2.3 GB) and expanded "
+                       "to bf16 (12.9 GB); 128 tokens per timing, CUDA graph replay",
+           "peak_source": f"{peak_kind} hbm_gbs"}
+    del keep, dl, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=False):
     """The q=4 verification and prefill sections named in --sections (cpu: add
     the oracle's prefill rate on the host to each prefill section)."""
@@ -702,6 +765,8 @@ def run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=False):
                                  hbm_peak, peak_kind, cpu))
     if pre:
         out["prefill"] = pre
+    if "ablation" in sec:
+        out["expand_then_multiply"] = bench_expanded(args, hbm_peak, peak_kind)
     if "stack" in sec:
         out["prefill_stack"], out["decode_stack"] = bench_stack(
             args, args.prefill_tokens or 32512, args.stack_layers, tc_peak, peak_kind)
@@ -895,8 +960,8 @@ def main():
     ap.add_argument("--replicas", type=int, default=8)
     ap.add_argument("--impl", default="moeq", choices=["moeq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sections", default="decode,verify,prefill,stack",
-                    help="comma list of decode, verify, prefill (= prefill3,prefill4), stack; "
+    ap.add_argument("--sections", default="decode,verify,prefill,ablation,stack",
+                    help="comma list of decode, verify, prefill (= prefill3,prefill4), ablation, stack; "
                          "without decode only the named sections run (profiling)")
     ap.add_argument("--stack-layers", type=int, default=43)
     ap.add_argument("--prefill-tokens", type=int, default=0,

@@ -97,6 +97,9 @@ def _declare(L):
         "moe_ffn_stack_prefill": (i, [P, i, P, i, P, P, sz, P, P]),
         "moe_ffn_stack_decode": (i, [P, i, P, P, P, sz, P, P]),
         "moe_quantize_expert": (i, [i, i, i, P, P, P, P, P, sz, P, P]),
+        "moe_expand_bf16": (i, [P, i, i, P, P]),
+        "moe_ffn_expanded_workspace": (sz, [i, i, i, i]),
+        "moe_ffn_decode_expanded": (i, [P, P, P, P, sz, P, P]),
         "h32_rotate": (i, [P, P, i, P, P]),
         "moe_rmsnorm_bf16": (i, [P, i, i, P, P]),
         "moeq_version": (C.c_char_p, []),
@@ -113,7 +116,8 @@ EXPORTED = ["moeq_packed_bytes", "moeq_validate_layer", "moe_ffn_workspace",
             "moe_ffn_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_ffn_decode",
             "moe_ffn_decode_static",
             "moe_ffn_verify_q4", "moe_ffn_prefill", "moe_ffn_stack_prefill", "moe_ffn_stack_decode",
-            "moe_quantize_expert", "h32_rotate",
+            "moe_quantize_expert", "moe_expand_bf16", "moe_ffn_expanded_workspace",
+            "moe_ffn_decode_expanded", "h32_rotate",
             "moe_rmsnorm_bf16",
             "moeq_version", "moeq_synth_codes", "moeq_synth_scales"]
 
@@ -205,6 +209,20 @@ def moe_quantize_expert(fmt, rows, cols, w, codes_u8, scales, codebook, ws, ws_b
     return _check("moe_quantize_expert", load().moe_quantize_expert(
         fmt, rows, cols, _ptr(w), _ptr(codes_u8), _ptr(scales), _ptr(codebook), _ptr(ws), ws_bytes,
         _ptr(dev_status), _stream(stream)))
+
+
+def moe_expand_bf16(matrix: MoeqMatrix, e0, ne, out_bf16, stream=None):
+    return _check("moe_expand_bf16", load().moe_expand_bf16(C.byref(matrix), e0, ne, _ptr(out_bf16),
+                                                            _stream(stream)))
+
+
+def moe_ffn_expanded_workspace(H, I, k, has_shared) -> int:
+    return load().moe_ffn_expanded_workspace(H, I, k, has_shared)
+
+
+def moe_ffn_decode_expanded(layer: MoeqLayer, x, y, ws, ws_bytes, dev_status=None, stream=None):
+    return _check("moe_ffn_decode_expanded", load().moe_ffn_decode_expanded(
+        C.byref(layer), _ptr(x), _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
 
 
 def moe_ffn_stack_decode(layers, x, r, ws, ws_bytes, dev_status=None, stream=None):

@@ -129,6 +129,28 @@ def build_layer(seed: int, layer: int, cfg: dict, device="cuda") -> DeviceLayer:
     return dl
 
 
+def expand_layer(dl: DeviceLayer, device="cuda"):
+    """The layer's packed matrices expanded to bf16 (moe_expand_bf16), as a
+    layer descriptor of MOEQ_BF16 matrices for moe_ffn_decode_expanded; returns
+    (descriptor, the tensors that hold the weights)."""
+    from . import MOEQ_BF16, moe_expand_bf16
+    keep = []
+    L = MoeqLayer()
+    src = dl.desc()
+    L.H, L.I, L.E, L.k, L.has_shared = src.H, src.I, src.E, src.k, src.has_shared
+    L.router = src.router
+    for name in ("gate", "up", "down", "sgate", "sup", "sdown"):
+        if name not in dl.mats:
+            continue
+        m = dl.mats[name]
+        out = torch.empty(m.E * m.rows * m.cols, dtype=torch.int16, device=device)
+        moe_expand_bf16(m.desc(), 0, m.E, out)
+        keep.append(out)
+        setattr(L, name, MoeqMatrix(MOEQ_BF16, m.rows, m.cols, m.E, out.data_ptr(), 2 * m.rows * m.cols,
+                                    None, 0, None, 0, 0))
+    return L, keep
+
+
 class Workspace:
     """A zeroed workspace for one FFN entry point (mode 0 decode, 1 q4, 2 prefill)."""
 

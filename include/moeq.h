@@ -202,6 +202,29 @@ int moe_quantize_expert(int fmt, int rows, int cols, const float* w, uint8_t* co
                         int8_t* codebook, void* ws, size_t ws_bytes, int32_t* dev_status,
                         moeq_stream stream);
 
+/* The "generic expand-then-multiply fallback" that "Lucebox x Geometric ...",
+ * section "Lucebox Engine integration with Geometric", measures the fused
+ * matvec against (2.2x), as an ablation on this GPU; not on the fused path.
+ *
+ * moe_expand_bf16: experts e0 .. e0+ne-1 of the packed matrix m to bf16
+ * weights out_bf16 [ne x rows x cols], w = bf16_rne(codebook[code] * block
+ * scale) (the product is exact in fp32). m is validated as a packed role;
+ * out_bf16 is device memory of the caller, 16-byte aligned.
+ *
+ * moe_ffn_decode_expanded: batch-1 decode of a layer whose gate, up, down
+ * (and shared) matrices are MOEQ_BF16 rows (codes = bf16 [rows x cols] per
+ * expert, expert_stride_codes bytes apart; scales and codebooks unused): the
+ * router and top-k of moe_route_topk, then per slot g = W_gate x, u = W_up x
+ * (bf16 weights, x as given, fp32 sums), h = silu(g) u in fp32 (no
+ * quantization), o = W_down h, y = sum_slot p o + o_shared in slot order.
+ * H a multiple of 256, I of 128, E <= 1024, no H32 rotation. ws: at least
+ * moe_ffn_expanded_workspace(H, I, k, has_shared) bytes of device memory.
+ * Three kernels enqueued on the stream. */
+int moe_expand_bf16(const moeq_matrix* m, int e0, int ne, uint16_t* out_bf16, moeq_stream stream);
+size_t moe_ffn_expanded_workspace(int H, int I, int k, int has_shared);
+int moe_ffn_decode_expanded(const moeq_layer* L, const uint16_t* x, float* y, void* ws, size_t ws_bytes,
+                            int32_t* dev_status, moeq_stream stream);
+
 /* Router and top-k for T tokens ("DeepSeek V4 Flash: 284B model ...", section
  * "Decode: up to 32 tok/s": routing with dedicated TOP_K kernels):
  * logits[t,e] = sum_h router[e,h] x[t,h] with bf16 operands and an fp32 sum in
