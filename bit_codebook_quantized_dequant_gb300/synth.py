@@ -199,19 +199,31 @@ WORKLOADS = {
             shared_fmt=4, h32=False, T=1, layers=1, dense=False),
     "decode-b1-fp2down": dict(name="decode-b1-fp2down", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=2,
             shared_fmt=4, h32=False, T=1, layers=1, dense=False),
+    "decode-b1-p24down": dict(name="decode-b1-p24down", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=24,
+            shared_fmt=4, h32=False, T=1, layers=1, dense=False),
     "prefill-h32-fp4": dict(name="prefill-h32-fp4", H=4096, I=2048, E=256, k=6, fmt_gu=4, fmt_down=4,
             shared_fmt=None, h32=True, T=2048, layers=1, dense=False),
     "prefill-43-layer-stack": dict(name="prefill-43-layer-stack", H=4096, I=2048, E=256, k=6, fmt_gu=2, fmt_down=3,
             shared_fmt=4, h32=False, T=32512, layers=43, dense=False),
 }
 WORKLOAD_ORDER = ("tiny-decode", "decode-b1", "verify-q4", "prefill-h32-fp4", "prefill-43-layer-stack",
-                  "decode-b1-top4", "decode-b1-fp2down")
+                  "decode-b1-top4", "decode-b1-fp2down", "decode-b1-p24down")
 
 # (role, rows-is-I?) for the matrices of a layer: gate/up are [I x H], down [H x I]
 MATRIX_ROLES = {
     "gate": ROLE_GATE, "up": ROLE_UP, "down": ROLE_DOWN,
     "sgate": ROLE_SGATE, "sup": ROLE_SUP, "sdown": ROLE_SDOWN, "dense": ROLE_DENSE,
 }
+
+
+# Format code of 3-bit codes in the Packed24 layout (the bit order differs
+# from FP3's; the drawn codes, scales and codebooks do not).
+FP3_PACKED24 = 24
+
+
+def code_bits(fmt: int) -> int:
+    """Bits per code of a format code."""
+    return 3 if fmt == FP3_PACKED24 else fmt
 
 
 def matrix_shape(cfg: dict, name: str):
@@ -241,18 +253,18 @@ def layer_roles(cfg: dict):
 
 def expert_codes(seed, layer, name, expert, cfg):
     fmt, rows, cols = matrix_shape(cfg, name)
-    return codes(seed, stream_id(layer, MATRIX_ROLES[name], expert, KIND_CODES), fmt, rows, cols)
+    return codes(seed, stream_id(layer, MATRIX_ROLES[name], expert, KIND_CODES), code_bits(fmt), rows, cols)
 
 
 def expert_scales(seed, layer, name, expert, cfg):
     fmt, rows, cols = matrix_shape(cfg, name)
-    return scales(seed, stream_id(layer, MATRIX_ROLES[name], expert, KIND_SCALES), fmt,
+    return scales(seed, stream_id(layer, MATRIX_ROLES[name], expert, KIND_SCALES), code_bits(fmt),
                   rows * (cols // 32))
 
 
 def expert_codebook(seed, layer, name, expert, cfg):
     fmt, _, _ = matrix_shape(cfg, name)
-    return codebook(seed, stream_id(layer, MATRIX_ROLES[name], expert, KIND_CODEBOOK), fmt)
+    return codebook(seed, stream_id(layer, MATRIX_ROLES[name], expert, KIND_CODEBOOK), code_bits(fmt))
 
 
 def router_weights(seed, layer, cfg):

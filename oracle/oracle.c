@@ -78,12 +78,22 @@ float orc_bf16_to_f32(uint16_t b) {
 /*   FP3: the low two bits as FP2 in w0, w1; bit 2 of element (w, h, n) at     */
 /*        bit 4n + p(w,h) of w2, with p(0,0)=2, p(0,1)=3, p(1,0)=0, p(1,1)=1.  */
 /*   FP4: element j has its 4-bit code in nibble j%8 of word j/8.             */
+/*   FP3, Packed24 layout (format code 24; the "Packed24 FP3" variant of      */
+/*        "deepseek-v4-flash-0731-evox3-rocm", section "The optimization      */
+/*        ladder", which names it only): the same 12 bytes, code j at bits   */
+/*        3j .. 3j+2 of the block read as one 96-bit little-endian integer,  */
+/*        i.e. 8 codes per 24 bits; its fp16 scale plane is FP3's.           */
 /* Weight value: scale(r, b) * codebook[code].                                */
 /* ------------------------------------------------------------------------ */
 
+#define ORC_FP3_PACKED24 24
+
 static int block_bytes(int fmt) {
-  return fmt == 2 ? 8 : fmt == 3 ? 12 : fmt == 4 ? 16 : -1;
+  return fmt == 2 ? 8 : fmt == 3 || fmt == ORC_FP3_PACKED24 ? 12 : fmt == 4 ? 16 : -1;
 }
+
+/* bits per code of a format code */
+static int code_bits(int fmt) { return fmt == ORC_FP3_PACKED24 ? 3 : fmt; }
 
 int orc_packed_bytes(int fmt, int rows, int cols, size_t* code_bytes, size_t* scale_bytes) {
   int bc = block_bytes(fmt);
@@ -105,7 +115,14 @@ static void wr32(uint8_t* p, uint32_t v) {
 static const int fp3_p[2][2] = {{2, 3}, {0, 1}}; /* p(w, h) */
 
 static void pack_block(int fmt, const uint8_t* c, uint8_t* out) {
-  if (fmt == 2 || fmt == 3) {
+  if (fmt == ORC_FP3_PACKED24) {
+    memset(out, 0, 12);
+    for (int j = 0; j < 32; j++)
+      for (int t = 0; t < 3; t++) {
+        int bit = 3 * j + t;
+        out[bit / 8] |= (uint8_t)(((c[j] >> t) & 1) << (bit % 8));
+      }
+  } else if (fmt == 2 || fmt == 3) {
     uint32_t w[2] = {0, 0}, hi = 0;
     for (int j = 0; j < 32; j++) {
       int wi = j >> 4, h = (j >> 3) & 1, n = j & 7;
@@ -125,7 +142,16 @@ static void pack_block(int fmt, const uint8_t* c, uint8_t* out) {
 }
 
 static void unpack_block(int fmt, const uint8_t* in, int* c) {
-  if (fmt == 2 || fmt == 3) {
+  if (fmt == ORC_FP3_PACKED24) {
+    for (int j = 0; j < 32; j++) {
+      int v = 0;
+      for (int t = 0; t < 3; t++) {
+        int bit = 3 * j + t;
+        v |= ((in[bit / 8] >> (bit % 8)) & 1) << t;
+      }
+      c[j] = v;
+    }
+  } else if (fmt == 2 || fmt == 3) {
     uint32_t w[2] = {rd32(in), rd32(in + 4)};
     uint32_t hi = fmt == 3 ? rd32(in + 8) : 0;
     for (int j = 0; j < 32; j++) {
@@ -144,7 +170,7 @@ int orc_pack(int fmt, int rows, int cols, const uint8_t* codes, uint8_t* out_cod
   if (bc < 0 || cols % 32 || rows < 0) return ORC_ERR_ARG;
   int nb = cols / 32;
   for (size_t i = 0; i < (size_t)rows * (size_t)cols; i++)
-    if (codes[i] >> fmt) return ORC_ERR_ARG;
+    if (codes[i] >> code_bits(fmt)) return ORC_ERR_ARG;
   for (int r = 0; r < rows; r++)
     for (int b = 0; b < nb; b++)
       pack_block(fmt, codes + (size_t)r * cols + 32 * b, out_codes + ((size_t)r * nb + b) * bc);

@@ -45,11 +45,11 @@ extern "C" {
  * to packed planes; entries for experts the caller did not materialize may be
  * NULL, and touching one returns ORC_ERR_MISSING. */
 typedef struct {
-  int fmt;            /* 2, 3 or 4 bits per code */
+  int fmt;            /* 2, 3 or 4 bits per code, or 24: 3-bit codes in the Packed24 layout */
   int rows, cols;     /* cols % 32 == 0 */
   const uint8_t* const* codes;  /* [E] code planes: rows x (cols/32) blocks */
   const void* const* scales;    /* [E] scale planes: fp16 bits (fmt 2,3) or E8M0 bytes (fmt 4) */
-  const int8_t* const* cb;      /* [E] codebooks of 2^fmt entries */
+  const int8_t* const* cb;      /* [E] codebooks of 2^bits entries */
 } orc_matrix;
 
 typedef struct {

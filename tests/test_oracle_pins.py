@@ -62,15 +62,15 @@ def test_scale_values():
 
 
 # ----------------------------------------------------------------- packing
-@pytest.mark.parametrize("fmt", [2, 3, 4])
+@pytest.mark.parametrize("fmt", [2, 3, 4, 24])
 def test_pack_roundtrip_and_sizes(fmt):
     for rows, cols in [(1, 32), (3, 128), (17, 256), (5, 4096)]:
-        c = S.codes(7, fmt * 100 + rows, fmt, rows, cols)
+        c = S.codes(7, fmt * 100 + rows, S.code_bits(fmt), rows, cols)
         p = O.pack(fmt, c)
         nb = rows * cols // 32
         cb, sb = O.packed_bytes(fmt, rows, cols)
-        assert cb == nb * {2: 8, 3: 12, 4: 16}[fmt]
-        assert cb + sb == nb * {2: 10, 3: 14, 4: 17}[fmt]
+        assert cb == nb * {2: 8, 3: 12, 4: 16, 24: 12}[fmt]
+        assert cb + sb == nb * {2: 10, 3: 14, 4: 17, 24: 14}[fmt]
         assert p.size == cb
         np.testing.assert_array_equal(O.unpack(fmt, rows, cols, p), c)
 
@@ -82,6 +82,22 @@ def test_pack_golden_bytes():
         assert O.pack(int(fmt), c).tobytes().hex() == hexbytes, (fmt, expr)
         n += 1
     assert n >= 9
+
+
+def test_packed24_bytes_against_a_96_bit_integer():
+    """Packed24: each block equals sum_j code_j * 8^j written as a 12-byte
+    little-endian integer (Python integers, not the oracle's bit loop), for
+    random codes over several blocks and rows."""
+    c = S.codes(9, 2424, 3, 7, 256)
+    p = O.pack(24, c).reshape(7, 8, 12)
+    for r in range(7):
+        for b in range(8):
+            v = sum(int(c[r, 32 * b + j]) << (3 * j) for j in range(32))
+            assert p[r, b].tobytes() == v.to_bytes(12, "little")
+    with pytest.raises(RuntimeError):
+        bad = np.zeros((1, 32), dtype=np.uint8)
+        bad[0, 3] = 8
+        O.pack(24, bad)
 
 
 def test_pack_rejects_out_of_range_codes():
@@ -302,11 +318,13 @@ def _brute_ffn(cfg, seed, L, x, idx_p):
     return y, np.stack(hqs)
 
 
-@pytest.mark.parametrize("variant", ["tiny", "tiny-shared", "tiny-h32"])
+@pytest.mark.parametrize("variant", ["tiny", "tiny-shared", "tiny-h32", "tiny-p24"])
 def test_ffn_decode_equals_brute_force(variant):
     cfg = dict(S.WORKLOADS["tiny-decode"])
     if variant == "tiny-shared":
         cfg.update(shared_fmt=4, k=3)
+    if variant == "tiny-p24":  # down projections in the Packed24 layout
+        cfg.update(fmt_down=24)
     if variant == "tiny-h32":
         cfg.update(h32=True, fmt_gu=4, fmt_down=4)
     seed = 21
