@@ -481,6 +481,23 @@ def test_quantizer_scales_codes_against_numpy(fmt):
     np.testing.assert_array_equal(codes, np.argmin(dist, axis=2))
 
 
+def test_quantizer_lloyd_steps_golden():
+    """A block whose codebook moves under the Lloyd steps, each step derived by
+    hand (tests/golden/quantizer_lloyd.txt): pins the mid-quantile start, the
+    nearest-entry cells with ties to the lower entry, and the half-up mean."""
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "quantizer_lloyd.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k] = v.split()
+    w = np.array([float(t) for t in vals["w"]], np.float32)[None, :]
+    codes, sc, cb = O.quantize_expert(2, w)
+    assert sc.ravel().tolist() == [int(vals["scale"][0], 16)]
+    assert cb.astype(int).tolist() == [int(t) for t in vals["codebook"]]
+    assert codes.ravel().tolist() == [int(t) for t in vals["codes"]]
+
+
 def test_quantizer_ties_go_to_the_lower_entry():
     # codebook {-127, -1, 1, 127}; zeros sit exactly between -1 and 1
     fmt, rows, cols = 2, 8, 256
