@@ -84,9 +84,22 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+DEVICE_HEADER = "bit_codebook_quantized_dequant_gb300/csrc/moeq_device.cuh"
+
+
+def source_sha(source: str) -> str:
+    """Hash of a kernel's source file and the device header it includes."""
+    h = hashlib.sha256()
+    for f in (source, DEVICE_HEADER):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _traffic(kernel: str, source: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel; else None."""
+    the current source of the kernel (its file and the device header); else
+    None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -95,9 +108,7 @@ def _traffic(kernel: str, source: str):
     ent = d.get(kernel)
     if not ent:
         return None
-    with open(os.path.join(ROOT, source), "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    return ent["bytes_per_launch"] if ent.get("source_sha") == h else None
+    return ent["bytes_per_launch"] if ent.get("source_sha") == source_sha(source) else None
 
 
 class ClockSampler:
@@ -626,6 +637,8 @@ def bench_stack(args, T, nlayers, tc_peak, peak_kind):
     del ws, r, r1
     torch.cuda.empty_cache()
     dec = bench_stack_decode(args, layers, cfg, seed)
+    torch.cuda.empty_cache()
+    dec["verify_q4_stack"] = bench_stack_verify(args, layers, cfg, seed)
     del layers
     torch.cuda.empty_cache()
     return out, dec
@@ -688,6 +701,86 @@ def bench_stack_decode(args, layers, cfg, seed):
                                       "oracle parity is a GPU test"}}
 
 
+def bench_stack_verify(args, layers, cfg, seed):
+    """q=4 through the whole stack (moe_ffn_stack_verify_q4: four columns,
+    each layer's weights read once per call for all of them), calls replayed
+    from CUDA graphs; the distinct experts of each (call, layer) are counted
+    afterwards by the same columns through the separate entry points, whose
+    result must equal the stack's bit for bit."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Debug, Workspace, to_dev_u16
+    nl = len(layers)
+    descs = [dl.desc() for dl in layers]
+    ws = Workspace(layers[0], 5)
+    H = cfg["H"]
+    nb = 16
+    X = S.tokens(seed, cfg, 4 * nb, start=8192)
+    xs = to_dev_u16(X)
+    r = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(i, s):
+        M.moe_ffn_stack_verify_q4(descs, xs.data_ptr() + (i % nb) * 4 * H * 2, r, ws.ptr, ws.nbytes, st, s)
+
+    warm, steps = 3, 8
+    for i in range(warm):
+        step(i, stream)
+    torch.cuda.synchronize()
+    graphs = capture_steps(step, warm, steps, stream, chunk=8)
+    replay(graphs, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(graphs, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    assert st.item() == 0, f"device status {st.item()}"
+    del graphs
+    # the timed calls' columns through the composition: distinct experts per
+    # (call, layer), and the last call's result against the stack's
+    ws1 = Workspace(layers[0], 1)
+    d = Debug(cfg, 4)
+    a = torch.zeros(4 * H, dtype=torch.int16, device="cuda")
+    y = torch.zeros(4 * H, dtype=torch.float32, device="cuda")
+    nbytes, ndist = 0.0, []
+    for j in range(steps):
+        b = (warm + j) % nb
+        rc = torch.from_numpy((X[4 * b:4 * b + 4].astype(np.uint32) << 16).view(np.float32).reshape(-1).copy()).cuda()
+        for l in range(nl):
+            M.moe_rmsnorm_bf16(rc, 4, H, a)
+            M.moe_ffn_verify_q4(descs[l], None, a, y, None, ws1.ptr, ws1.nbytes, st, d.struct)
+            nd = len(set(d.t["idx"].cpu().tolist()))
+            ndist.append(nd)
+            nbytes += algorithmic_bytes_verify(cfg, nd)
+            rc += y
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"device status {st.item()}"
+    same = bool(torch.equal(rc, r))
+    per_call = nbytes / steps
+    hbm_peak, _, peak_kind = _peaks()
+    achieved = per_call / (ms * 1e-3) / 1e9
+    return {"metric": f"q=4 verification column-tok/s ({nl}-layer stack)", "value": 4.0 / (ms * 1e-3),
+            "unit": "column-tok/s", "ms_per_call": ms, "calls_timed": steps, "layers": nl,
+            "distinct_experts_per_layer_call": float(np.mean(ndist)),
+            "workload": f"prefill-43-layer-stack layers (decode-b1 shapes), 4 independently routed "
+                        f"columns through all {nl} layers per call: RMSNorm + q=4 FFN (no dense "
+                        f"projection) + fp32 residual per layer",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": per_call},
+            "gpu_launches_per_call": 2 * nl + 1, "launch": "CUDA graph replay",
+            "parity_after": {"composition_bit_equal": same,
+                             "check": "the last timed call's columns through RMSNorm, q=4 and the "
+                                      "residual as separate calls equal the stack's output bit for "
+                                      "bit; per-column equality with the decode stack and its "
+                                      "oracle parity are GPU tests"}}
+
+
 def bench_expanded(args, hbm_peak, peak_kind):
     """The expand-then-multiply ablation: one decode layer expanded to bf16
     (12.9 GB), decoded with moe_ffn_decode_expanded, beside the fused decode
@@ -705,7 +798,7 @@ def bench_expanded(args, hbm_peak, peak_kind):
     xs = to_dev_u16(S.tokens(seed, cfg, ntok, start=2048))
     y = torch.zeros(H, dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wsx_b = M.moe_ffn_expanded_workspace(H, I, k, 1)
+    wsx_b = M.moe_ffn_expanded_workspace(H, I, cfg["E"], k, 1)
     wsx = torch.zeros(wsx_b, dtype=torch.uint8, device="cuda")
     ws = Workspace(dl, 0)
     desc = dl.desc()
@@ -749,6 +842,70 @@ def bench_expanded(args, hbm_peak, peak_kind):
     return res
 
 
+def bench_packed24(args, hbm_peak, peak_kind):
+    """Layout A/B on the decode's integer-pipe budget: one decode-b1 layer with
+    its routed down projections in FP3's planes and the same codes, scales and
+    codebooks in the Packed24 layout (the same bytes); both decoded from CUDA
+    graphs on the same tokens, three alternating rounds each."""
+    import torch
+    import bit_codebook_quantized_dequant_gb300 as M
+    from bit_codebook_quantized_dequant_gb300 import synth as S
+    from bit_codebook_quantized_dequant_gb300.workload import Workspace, build_layer, to_dev_u16
+    cfg3 = S.WORKLOADS[DECODE_WORKLOAD]
+    cfg24 = dict(cfg3, fmt_down=S.FP3_PACKED24)
+    seed = S.workload_seed(DECODE_WORKLOAD)
+    H = cfg3["H"]
+    ntok = 256
+    xs = to_dev_u16(S.tokens(seed, cfg3, ntok, start=3072))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    arms = {}
+    for name, cfg in (("fp3", cfg3), ("packed24", cfg24)):
+        dl = build_layer(seed, 6, cfg)
+        ws = Workspace(dl, 0)
+        y = torch.zeros(H, dtype=torch.float32, device="cuda")
+        arms[name] = (dl, ws, y, dl.desc())
+    steps = 128
+    graphs = {}
+    for name, (dl, ws, y, desc) in arms.items():
+        def fn(i, s, desc=desc, ws=ws, y=y):
+            M.moe_ffn_decode(desc, xs.data_ptr() + (i % ntok) * H * 2, y, ws.ptr, ws.nbytes, st, None, s)
+        for i in range(5):
+            fn(i, stream)
+        torch.cuda.synchronize()
+        graphs[name] = capture_steps(fn, 5, steps, stream)
+    times = {n: [] for n in arms}
+    for _ in range(3):
+        for name in arms:
+            replay(graphs[name], stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            replay(graphs[name], stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[name].append(e0.elapsed_time(e1) / steps * 1e3)
+    del graphs
+    assert st.item() == 0, f"device status {st.item()}"
+    same = bool(torch.equal(arms["fp3"][2], arms["packed24"][2]))
+    us = {n: statistics.median(t) for n, t in times.items()}
+    res = {"metric": "Packed24 layout A/B: decode us/token, routed down projections in FP3 planes "
+                     "vs the Packed24 bit order (same codes and bytes)",
+           "us_fp3": us["fp3"], "us_packed24": us["packed24"],
+           "packed24_slowdown": us["packed24"] / us["fp3"], "rounds_us": times,
+           "bytes_per_token": algorithmic_bytes_decode(cfg3),
+           "hbm_frac_fp3": algorithmic_bytes_decode(cfg3) / (us["fp3"] * 1e-6) / 1e9 / hbm_peak,
+           "hbm_frac_packed24": algorithmic_bytes_decode(cfg3) / (us["packed24"] * 1e-6) / 1e9 / hbm_peak,
+           "workload": "one decode-b1 layer (replica 6) in each layout; 128 tokens per timing, median "
+                       "of 3 alternating rounds, CUDA graph replay",
+           "parity_after": {"last_token_bit_equal": same,
+                            "check": "the last timed token's y from the two layouts is equal bit for bit"},
+           "peak_source": f"{peak_kind} hbm_gbs"}
+    del arms
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=False):
     """The q=4 verification and prefill sections named in --sections (cpu: add
     the oracle's prefill rate on the host to each prefill section)."""
@@ -767,6 +924,7 @@ def run_sections(args, hbm_peak, tc_peak, peak_kind, cpu=False):
         out["prefill"] = pre
     if "ablation" in sec:
         out["expand_then_multiply"] = bench_expanded(args, hbm_peak, peak_kind)
+        out["packed24_layout"] = bench_packed24(args, hbm_peak, peak_kind)
     if "stack" in sec:
         out["prefill_stack"], out["decode_stack"] = bench_stack(
             args, args.prefill_tokens or 32512, args.stack_layers, tc_peak, peak_kind)

@@ -15,7 +15,7 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoeq.so")
 
-MOEQ_FP2, MOEQ_FP3, MOEQ_FP4, MOEQ_BF16 = 2, 3, 4, 16
+MOEQ_FP2, MOEQ_FP3, MOEQ_FP4, MOEQ_BF16, MOEQ_FP3_PACKED24 = 2, 3, 4, 16, 24
 STATUS = {
     0: "MOEQ_OK", -1: "MOEQ_ERR_ARG", -2: "MOEQ_ERR_SHAPE", -3: "MOEQ_ERR_ALIGN",
     -4: "MOEQ_ERR_FORMAT", -5: "MOEQ_ERR_CODEBOOK_MISSING", -6: "MOEQ_ERR_CODEBOOK_TRUNCATED",
@@ -96,9 +96,10 @@ def _declare(L):
                                 P]),
         "moe_ffn_stack_prefill": (i, [P, i, P, i, P, P, sz, P, P]),
         "moe_ffn_stack_decode": (i, [P, i, P, P, P, sz, P, P]),
+        "moe_ffn_stack_verify_q4": (i, [P, i, P, P, P, sz, P, P]),
         "moe_quantize_expert": (i, [i, i, i, P, P, P, P, P, sz, P, P]),
         "moe_expand_bf16": (i, [P, i, i, P, P]),
-        "moe_ffn_expanded_workspace": (sz, [i, i, i, i]),
+        "moe_ffn_expanded_workspace": (sz, [i, i, i, i, i]),
         "moe_ffn_decode_expanded": (i, [P, P, P, P, sz, P, P]),
         "h32_rotate": (i, [P, P, i, P, P]),
         "moe_rmsnorm_bf16": (i, [P, i, i, P, P]),
@@ -116,7 +117,7 @@ EXPORTED = ["moeq_packed_bytes", "moeq_validate_layer", "moe_ffn_workspace",
             "moe_ffn_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_ffn_decode",
             "moe_ffn_decode_static",
             "moe_ffn_verify_q4", "moe_ffn_prefill", "moe_ffn_stack_prefill", "moe_ffn_stack_decode",
-            "moe_quantize_expert", "moe_expand_bf16", "moe_ffn_expanded_workspace",
+            "moe_ffn_stack_verify_q4", "moe_quantize_expert", "moe_expand_bf16", "moe_ffn_expanded_workspace",
             "moe_ffn_decode_expanded", "h32_rotate",
             "moe_rmsnorm_bf16",
             "moeq_version", "moeq_synth_codes", "moeq_synth_scales"]
@@ -216,8 +217,8 @@ def moe_expand_bf16(matrix: MoeqMatrix, e0, ne, out_bf16, stream=None):
                                                             _stream(stream)))
 
 
-def moe_ffn_expanded_workspace(H, I, k, has_shared) -> int:
-    return load().moe_ffn_expanded_workspace(H, I, k, has_shared)
+def moe_ffn_expanded_workspace(H, I, E, k, has_shared) -> int:
+    return load().moe_ffn_expanded_workspace(H, I, E, k, has_shared)
 
 
 def moe_ffn_decode_expanded(layer: MoeqLayer, x, y, ws, ws_bytes, dev_status=None, stream=None):
@@ -229,6 +230,13 @@ def moe_ffn_stack_decode(layers, x, r, ws, ws_bytes, dev_status=None, stream=Non
     """layers: a sequence of MoeqLayer (copied into one contiguous array)."""
     arr = (MoeqLayer * len(layers))(*layers)
     return _check("moe_ffn_stack_decode", load().moe_ffn_stack_decode(
+        arr, len(layers), _ptr(x), _ptr(r), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def moe_ffn_stack_verify_q4(layers, x, r, ws, ws_bytes, dev_status=None, stream=None):
+    """layers: a sequence of MoeqLayer; x [4 x H] bf16, r [4 x H] fp32."""
+    arr = (MoeqLayer * len(layers))(*layers)
+    return _check("moe_ffn_stack_verify_q4", load().moe_ffn_stack_verify_q4(
         arr, len(layers), _ptr(x), _ptr(r), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
 
 

@@ -12,7 +12,7 @@
 namespace moeq {
 
 int validate_matrix(const moeq_matrix& m, int rows, int cols, int experts) {
-  if (m.fmt != 2 && m.fmt != 3 && m.fmt != 4) return MOEQ_ERR_FORMAT;
+  if (m.fmt != 2 && m.fmt != 3 && m.fmt != 4 && m.fmt != MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;
   if (m.rows != rows || m.cols != cols || m.num_experts != experts) return MOEQ_ERR_SHAPE;
   if (cols <= 0 || rows <= 0 || cols % 128 != 0) return MOEQ_ERR_SHAPE;
   if (!m.codes || !m.scales) return MOEQ_ERR_ARG;
@@ -24,7 +24,7 @@ int validate_matrix(const moeq_matrix& m, int rows, int cols, int experts) {
     if (m.expert_stride_codes < cbytes || m.expert_stride_scales < sbytes) return MOEQ_ERR_SHAPE;
   }
   if (!m.codebooks) return MOEQ_ERR_CODEBOOK_MISSING;
-  const int need = 1 << m.fmt;
+  const int need = 1 << fmt_code_bits(m.fmt);
   if (m.cb_len < need) return MOEQ_ERR_CODEBOOK_TRUNCATED;
   if (m.cb_len > need) return MOEQ_ERR_CODEBOOK_MISMATCH;
   if (experts > 1 && m.cb_stride < m.cb_len) return MOEQ_ERR_CODEBOOK_DUPLICATE;
@@ -45,11 +45,14 @@ int validate_layer(const moeq_layer* L) {
   if ((rc = validate_matrix(L->up, I, H, E))) return rc;
   if ((rc = validate_matrix(L->down, H, I, E))) return rc;
   if (L->gate.fmt != L->up.fmt) return MOEQ_ERR_FORMAT;
+  // the Packed24 layout is decoded for the routed down projection only
+  if (L->gate.fmt == MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;
   if (L->has_shared) {
     if ((rc = validate_matrix(L->sgate, I, H, 1))) return rc;
     if ((rc = validate_matrix(L->sup, I, H, 1))) return rc;
     if ((rc = validate_matrix(L->sdown, H, I, 1))) return rc;
     if (L->sgate.fmt != L->sup.fmt) return MOEQ_ERR_FORMAT;
+    if (L->sgate.fmt == MOEQ_FP3_PACKED24 || L->sdown.fmt == MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;
   }
   return MOEQ_OK;
 }
@@ -84,7 +87,7 @@ extern "C" int moeq_packed_bytes(int fmt, int rows, int cols, size_t* code_bytes
     if (scale_bytes) *scale_bytes = 0;
     return MOEQ_OK;
   }
-  if (fmt != 2 && fmt != 3 && fmt != 4) return MOEQ_ERR_FORMAT;
+  if (fmt != 2 && fmt != 3 && fmt != 4 && fmt != MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;
   if (rows < 0 || cols < 0 || cols % 32) return MOEQ_ERR_SHAPE;
   const size_t nblk = static_cast<size_t>(rows) * (cols / 32);
   if (code_bytes) *code_bytes = nblk * fmt_block_bytes(fmt);
@@ -102,6 +105,9 @@ extern "C" size_t moe_ffn_workspace(const moeq_layer* L, int T_max, int mode) {
   if (mode == 4)  // decode stack of layers shaped like L: decode workspace + a [H] bf16 + y [H] fp32
     return decode_ws_layout(L->H, L->I, L->E, L->k, L->has_shared).total + align256(2 * static_cast<size_t>(L->H)) +
            align256(4 * static_cast<size_t>(L->H));
+  if (mode == 5)  // q=4 stack: q=4 workspace + a [4 x H] bf16 + y [4 x H] fp32
+    return verify_ws_layout(L->H, L->I, L->E, L->k, L->has_shared).total + align256(8 * static_cast<size_t>(L->H)) +
+           align256(16 * static_cast<size_t>(L->H));
   if (mode == 3)  // a stack of layers shaped like L: prefill workspace + the bf16 RMSNorm output
     return prefill_ws_layout(L->H, L->I, L->E, L->k, L->has_shared, T_max).total +
            align256(2 * static_cast<size_t>(T_max) * L->H);

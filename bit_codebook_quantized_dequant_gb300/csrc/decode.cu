@@ -191,7 +191,7 @@ struct StageMap {
 __host__ __device__ __forceinline__ uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
 
 __host__ __device__ __forceinline__ uint32_t code_pitch(int fmt, int K) {
-  return static_cast<uint32_t>(K / 32) * (fmt == 2 ? 8 : fmt == 3 ? 12 : 16);
+  return static_cast<uint32_t>(K / 32) * (fmt == 2 ? 8 : fmt == 3 || fmt == MOEQ_FP3_PACKED24 ? 12 : 16);
 }
 __host__ __device__ __forceinline__ uint32_t scale_pitch(int fmt, int K) {
   return static_cast<uint32_t>(K / 32) * (fmt == 4 ? 1 : 2);
@@ -962,6 +962,7 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem<COLS>& sm, int s, i
     float o1[R];
     if (fmt == 2) down_rows<2, DBG>(a, st, mp, cb, wg, lane, un.chunk, c0, vec, o1);
     else if (fmt == 3) down_rows<3, DBG>(a, st, mp, cb, wg, lane, un.chunk, c0, vec, o1);
+    else if (fmt == MOEQ_FP3_PACKED24) down_rows<MOEQ_FP3_PACKED24, DBG>(a, st, mp, cb, wg, lane, un.chunk, c0, vec, o1);
     else down_rows<4, DBG>(a, st, mp, cb, wg, lane, un.chunk, c0, vec, o1);
 #pragma unroll
     for (int j = 0; j < R; ++j) o[j * COLS] = o1[j];
@@ -976,6 +977,8 @@ __device__ void compute_unit(const DecodeArgs& a, DecodeSmem<COLS>& sm, int s, i
       rows_cols<2, DBG, COLS, true>(a, st, mp.ca, mp.sa, nb, act, a.I, st + mp.sb, a.hd_stride, nullptr, cb, wg, lane, row0, vec, o);
     else if (fmt == 3)
       rows_cols<3, DBG, COLS, true>(a, st, mp.ca, mp.sa, nb, act, a.I, st + mp.sb, a.hd_stride, nullptr, cb, wg, lane, row0, vec, o);
+    else if (fmt == MOEQ_FP3_PACKED24)
+      rows_cols<MOEQ_FP3_PACKED24, DBG, COLS, true>(a, st, mp.ca, mp.sa, nb, act, a.I, st + mp.sb, a.hd_stride, nullptr, cb, wg, lane, row0, vec, o);
     else
       rows_cols<4, DBG, COLS, true>(a, st, mp.ca, mp.sa, nb, act, a.I, st + mp.sb, a.hd_stride, nullptr, cb, wg, lane, row0, vec, o);
   }
@@ -1313,6 +1316,7 @@ extern "C" int moe_ffn_verify_q4(const moeq_layer* L, const moeq_matrix* dense, 
   if (dense) {
     rc = validate_matrix(*dense, dense->rows, L->H, 1);
     if (rc) return rc;
+    if (dense->fmt == MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;
     if (dense->rows % kDownRows) return MOEQ_ERR_SHAPE;
     if (dense_map(dense->fmt, L->H).total > static_cast<uint32_t>(kStageBytes)) return MOEQ_ERR_SHAPE;
     if (!y_dense) return MOEQ_ERR_ARG;
@@ -1437,10 +1441,41 @@ extern "C" int moe_ffn_stack_decode(const moeq_layer* layers, int nlayers, const
   float* y = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + need + abytes);
   // r_0 = float(x), a_0 = RMSNorm(r_0); per layer y = FFN_l(a_l), then
   // r_{l+1} = r_l + y and a_{l+1} = RMSNorm(r_{l+1}) (no norm after the last)
-  int rc = stack_step_launch(x, nullptr, r, a, H, s);
+  int rc = stack_step_launch(x, nullptr, r, a, H, 1, s);
   for (int l = 0; l < nlayers && !rc; ++l) {
     rc = moe_ffn_decode(&layers[l], a, y, ws, need, dev_status, nullptr, stream);
-    if (!rc) rc = stack_step_launch(nullptr, y, r, l + 1 < nlayers ? a : nullptr, H, s);
+    if (!rc) rc = stack_step_launch(nullptr, y, r, l + 1 < nlayers ? a : nullptr, H, 1, s);
+  }
+  return rc;
+}
+
+extern "C" int moe_ffn_stack_verify_q4(const moeq_layer* layers, int nlayers, const uint16_t* x, float* r,
+                                       void* ws, size_t ws_bytes, int32_t* dev_status, moeq_stream stream) {
+  if (!layers || nlayers < 1) return MOEQ_ERR_ARG;
+  const int H = layers[0].H;
+  size_t need = 0;
+  for (int l = 0; l < nlayers; ++l) {
+    const int rc = validate_layer(&layers[l]);
+    if (rc) return rc;
+    if (layers[l].H != H) return MOEQ_ERR_SHAPE;
+    if (!shapes_fit(&layers[l], 4)) return MOEQ_ERR_SHAPE;
+    const DecodeWs wl =
+        verify_ws_layout(layers[l].H, layers[l].I, layers[l].E, layers[l].k, layers[l].has_shared);
+    need = wl.total > need ? wl.total : need;
+  }
+  if (!x || !r) return MOEQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(r)) return MOEQ_ERR_ALIGN;
+  const size_t abytes = align256(8 * static_cast<size_t>(H)), ybytes = align256(16 * static_cast<size_t>(H));
+  if (!ws || !aligned16(ws) || ws_bytes < need + abytes + ybytes) return MOEQ_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint16_t* a = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + need);
+  float* y = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + need + abytes);
+  // the decode stack's recurrence on each of the 4 columns; each layer's
+  // weights are streamed once for all of them
+  int rc = stack_step_launch(x, nullptr, r, a, H, 4, s);
+  for (int l = 0; l < nlayers && !rc; ++l) {
+    rc = moe_ffn_verify_q4(&layers[l], nullptr, a, y, nullptr, ws, need, dev_status, nullptr, stream);
+    if (!rc) rc = stack_step_launch(nullptr, y, r, l + 1 < nlayers ? a : nullptr, H, 4, s);
   }
   return rc;
 }

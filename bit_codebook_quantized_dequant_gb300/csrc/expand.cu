@@ -64,6 +64,72 @@ struct XArgs {
   float* y;
 };
 
+// Router logits of one token, one warp per expert row in the canonical order
+// (lane j sums k = 256 i + 8 j + t over i, t with exact bf16 products, then
+// the combining rounds 16 .. 1), spread over the grid; the last CTA to arrive
+// takes the top-k and the softmax weights with one warp and returns the
+// arrival counter to zero for the next call.
+constexpr int kRouteWarps = 8;
+
+template <int NPL>
+__device__ __forceinline__ void last_cta_topk(const float* logits, int E, int k, int lane, int32_t* idx, float* p) {
+  float v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldcg(logits + e) : 0.0f;
+  }
+  int id;
+  float w;
+  warp_topk<NPL>(v, E, k, lane, id, w);
+  if (lane < k) {
+    idx[lane] = id;
+    p[lane] = w;
+  }
+}
+
+__global__ void __launch_bounds__(kRouteWarps * 32) xroute_kernel(const uint16_t* __restrict__ x,
+                                                                   const uint16_t* __restrict__ router, int E, int H,
+                                                                   int k, float* logits, uint32_t* arrive,
+                                                                   int32_t* idx, float* p) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  if (e < E) {
+    const uint16_t* wrow = router + static_cast<size_t>(e) * H;
+    float acc = 0.0f;
+    for (int i = 0; i < H / 256; ++i) {
+      const int k0 = 256 * i + 8 * lane;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow + k0));
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + k0));
+      acc = fmaf(bf16_lo(xv.x), bf16_lo(w.x), acc);
+      acc = fmaf(bf16_hi(xv.x), bf16_hi(w.x), acc);
+      acc = fmaf(bf16_lo(xv.y), bf16_lo(w.y), acc);
+      acc = fmaf(bf16_hi(xv.y), bf16_hi(w.y), acc);
+      acc = fmaf(bf16_lo(xv.z), bf16_lo(w.z), acc);
+      acc = fmaf(bf16_hi(xv.z), bf16_hi(w.z), acc);
+      acc = fmaf(bf16_lo(xv.w), bf16_lo(w.w), acc);
+      acc = fmaf(bf16_hi(xv.w), bf16_hi(w.w), acc);
+    }
+    acc = warp_sum_canonical(acc);
+    if (lane == 0) {
+      logits[e] = acc;
+      __threadfence();  // the logit is visible device-wide before this CTA arrives
+    }
+  }
+  __shared__ uint32_t last;
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(arrive, 1u) == gridDim.x - 1 ? 1u : 0u;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();  // every CTA's logits after seeing the last arrival
+  if (threadIdx.x < 32) {
+    if (E <= 256) last_cta_topk<8>(logits, E, k, lane, idx, p);
+    else if (E <= 512) last_cta_topk<16>(logits, E, k, lane, idx, p);
+    else last_cta_topk<32>(logits, E, k, lane, idx, p);
+    if (lane == 0) *arrive = 0u;
+  }
+}
+
 __device__ __forceinline__ float bf16x8_dot(const uint4 w, const float* v, float acc) {
   const float4 a = *reinterpret_cast<const float4*>(v);
   const float4 b = *reinterpret_cast<const float4*>(v + 4);
@@ -177,15 +243,18 @@ extern "C" int moe_expand_bf16(const moeq_matrix* m, int e0, int ne, uint16_t* o
     expand_kernel<2><<<grid, 256, 0, s>>>(d, e0, ne, out_bf16);
   else if (d.fmt == 3)
     expand_kernel<3><<<grid, 256, 0, s>>>(d, e0, ne, out_bf16);
+  else if (d.fmt == MOEQ_FP3_PACKED24)
+    expand_kernel<MOEQ_FP3_PACKED24><<<grid, 256, 0, s>>>(d, e0, ne, out_bf16);
   else
     expand_kernel<4><<<grid, 256, 0, s>>>(d, e0, ne, out_bf16);
   return cuda_status(cudaGetLastError());
 }
 
-extern "C" size_t moe_ffn_expanded_workspace(int H, int I, int k, int has_shared) {
-  if (H <= 0 || I <= 0 || k < 1 || k > kMaxTopK) return 0;
+// Workspace: idx [k], p [k], the arrival counter, logits [E], h [(k + shared) x I].
+extern "C" size_t moe_ffn_expanded_workspace(int H, int I, int E, int k, int has_shared) {
+  if (H <= 0 || I <= 0 || E < 1 || E > 1024 || k < 1 || k > kMaxTopK || k > E) return 0;
   (void)H;
-  return align256(4 * static_cast<size_t>(kMaxTopK)) * 2 +
+  return align256(4 * static_cast<size_t>(kMaxTopK)) * 3 + align256(4 * static_cast<size_t>(E)) +
          align256(4 * static_cast<size_t>(k + (has_shared ? 1 : 0)) * I);
 }
 
@@ -206,7 +275,7 @@ extern "C" int moe_ffn_decode_expanded(const moeq_layer* L, const uint16_t* x, f
   if (L->has_shared && ((rc = check_bf16_matrix(L->sgate, I, H, 1)) || (rc = check_bf16_matrix(L->sup, I, H, 1)) ||
                         (rc = check_bf16_matrix(L->sdown, H, I, 1))))
     return rc;
-  const size_t need = moe_ffn_expanded_workspace(H, I, k, L->has_shared);
+  const size_t need = moe_ffn_expanded_workspace(H, I, E, k, L->has_shared);
   if (!ws || !aligned16(ws) || ws_bytes < need) return MOEQ_ERR_WORKSPACE;
   const int ns = k + (L->has_shared ? 1 : 0);
   const size_t hsmem = 4 * static_cast<size_t>(ns) * I;
@@ -227,15 +296,19 @@ extern "C" int moe_ffn_decode_expanded(const moeq_layer* L, const uint16_t* x, f
     a.sup = static_cast<const uint16_t*>(L->sup.codes);
     a.sdown = static_cast<const uint16_t*>(L->sdown.codes);
   }
+  const size_t rec = align256(4 * static_cast<size_t>(kMaxTopK));
   int32_t* idx = reinterpret_cast<int32_t*>(w);
-  float* p = reinterpret_cast<float*>(w + align256(4 * static_cast<size_t>(kMaxTopK)));
+  float* p = reinterpret_cast<float*>(w + rec);
+  uint32_t* arrive = reinterpret_cast<uint32_t*>(w + 2 * rec);
+  float* logits = reinterpret_cast<float*>(w + 3 * rec);
   a.idx = idx;
   a.p = p;
-  a.h = reinterpret_cast<float*>(w + 2 * align256(4 * static_cast<size_t>(kMaxTopK)));
+  a.h = reinterpret_cast<float*>(w + 3 * rec + align256(4 * static_cast<size_t>(E)));
   a.y = y;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  rc = route_topk_launch(x, 1, L->router, E, H, k, idx, p, nullptr, s);
-  if (rc) return rc;
+  xroute_kernel<<<(E + kRouteWarps - 1) / kRouteWarps, kRouteWarps * 32, 0, s>>>(x, L->router, E, H, k, logits,
+                                                                                 arrive, idx, p);
+  if ((rc = cuda_status(cudaGetLastError()))) return rc;
   static thread_local int configured_dev = -1;
   if (configured_dev != di.device) {
     const int lim = static_cast<int>(di.max_smem_optin);

@@ -228,6 +228,36 @@ __device__ __forceinline__ int dot_fp3(uint32_t w0, uint32_t w1, uint32_t w2, ui
   return s + s2;
 }
 
+// FP3 in the Packed24 layout: code j at bits 3j..3j+2 of the 12-byte block
+// read as one 96-bit little-endian integer, 8 codes per 24 bits. Each 24-bit
+// group is spread into 8 selector nibbles: 6-bit code pairs into bytes, then
+// the two codes of each byte into its two nibbles.
+__device__ __forceinline__ uint32_t p24_spread(uint32_t u) {
+  const uint32_t t = (u & 0x3Fu) | ((u << 2) & 0x3F00u) | ((u << 4) & 0x3F0000u) | ((u << 6) & 0x3F000000u);
+  return (t & 0x07070707u) | ((t << 1) & 0x70707070u);
+}
+
+__device__ __forceinline__ Fp3Sel p24_selectors(uint32_t w0, uint32_t w1, uint32_t w2) {
+  Fp3Sel s;  // s00, s01, s10, s11 = codes 0..7, 8..15, 16..23, 24..31
+  s.s00 = p24_spread(w0);
+  s.s01 = p24_spread(__funnelshift_r(w0, w1, 24));
+  s.s10 = p24_spread(__funnelshift_r(w1, w2, 16));
+  s.s11 = p24_spread(w2 >> 8);
+  return s;
+}
+
+__device__ __forceinline__ int dot_fp3_sel(const Fp3Sel& t, uint32_t cb0, uint32_t cb1, const int* q) {
+  int s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s00)), q[0], 0);
+  int s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s00 >> 16)), q[1], 0);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s01)), q[2], s);
+  s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s01 >> 16)), q[3], s2);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s10)), q[4], s);
+  s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s10 >> 16)), q[5], s2);
+  s = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s11)), q[6], s);
+  s2 = __dp4a(static_cast<int>(prmt(cb0, cb1, t.s11 >> 16)), q[7], s2);
+  return s + s2;
+}
+
 // FP4 expansion of one word (8 codes in nibbles) into two words of int8 values.
 // Entries 0..7 and 8..15 are looked up with 3-bit selectors; bit 3 of each code
 // becomes a 0x00/0xff byte mask by a sign-replicating permute (selector nibble
@@ -272,6 +302,9 @@ __device__ __forceinline__ int block_dot(const uint8_t* p, const uint32_t* cb, c
   } else if constexpr (FMT == 3) {
     const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
     return dot_fp3(w[0], w[1], w[2], cb[0], cb[1], q);
+  } else if constexpr (FMT == MOEQ_FP3_PACKED24) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+    return dot_fp3_sel(p24_selectors(w[0], w[1], w[2]), cb[0], cb[1], q);
   } else {
     return dot_fp4(*reinterpret_cast<const uint4*>(p), cb, q);
   }
@@ -289,9 +322,9 @@ __device__ __forceinline__ void block_expand(const uint8_t* p, const uint32_t* c
     v[2] = prmt(cb[0], cb[0], b0); v[3] = prmt(cb[0], cb[0], b0 >> 16);
     v[4] = prmt(cb[0], cb[0], a1); v[5] = prmt(cb[0], cb[0], a1 >> 16);
     v[6] = prmt(cb[0], cb[0], b1); v[7] = prmt(cb[0], cb[0], b1 >> 16);
-  } else if constexpr (FMT == 3) {
+  } else if constexpr (FMT == 3 || FMT == MOEQ_FP3_PACKED24) {
     const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
-    const Fp3Sel t = fp3_selectors(w[0], w[1], w[2]);
+    const Fp3Sel t = FMT == 3 ? fp3_selectors(w[0], w[1], w[2]) : p24_selectors(w[0], w[1], w[2]);
     v[0] = prmt(cb[0], cb[1], t.s00); v[1] = prmt(cb[0], cb[1], t.s00 >> 16);
     v[2] = prmt(cb[0], cb[1], t.s01); v[3] = prmt(cb[0], cb[1], t.s01 >> 16);
     v[4] = prmt(cb[0], cb[1], t.s10); v[5] = prmt(cb[0], cb[1], t.s10 >> 16);
@@ -319,7 +352,7 @@ __device__ __forceinline__ int dot8(const uint32_t (&v)[8], const int* q) {
 
 template <int FMT>
 __host__ __device__ constexpr int block_bytes() {
-  return FMT == 2 ? 8 : FMT == 3 ? 12 : 16;
+  return FMT == 2 ? 8 : FMT == 3 || FMT == MOEQ_FP3_PACKED24 ? 12 : 16;
 }
 
 template <int FMT>

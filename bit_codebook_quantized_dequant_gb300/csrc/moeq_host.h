@@ -21,7 +21,10 @@ struct DMat {
   int rows, cols, fmt;
 };
 
-inline int fmt_block_bytes(int fmt) { return fmt == 2 ? 8 : fmt == 3 ? 12 : fmt == 4 ? 16 : 0; }
+inline int fmt_block_bytes(int fmt) {
+  return fmt == 2 ? 8 : fmt == 3 || fmt == MOEQ_FP3_PACKED24 ? 12 : fmt == 4 ? 16 : 0;
+}
+inline int fmt_code_bits(int fmt) { return fmt == MOEQ_FP3_PACKED24 ? 3 : fmt; }
 inline int fmt_scale_bytes(int fmt) { return fmt == 4 ? 1 : 2; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -84,9 +87,10 @@ struct TcGemm {
 };
 int tc_grouped_gemm(const TcGemm& g, cudaStream_t s);
 
-// One step of a decode stack on one token (route.cu): r = float(x) if x, else
-// r += y if y; then a = RMSNorm(r) if a. One warp.
-int stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, cudaStream_t s);
+// One step of a decode stack on `rows` tokens (route.cu), row by row: r =
+// float(x) if x, else r += y if y; then a = RMSNorm(r) if a. One warp a row.
+int stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, int rows,
+                      cudaStream_t s);
 
 // Router + top-k of T tokens enqueued on s (route.cu).
 int route_topk_launch(const uint16_t* x, int T, const uint16_t* router, int E, int H, int k,

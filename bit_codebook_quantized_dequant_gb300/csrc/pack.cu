@@ -22,7 +22,7 @@ __global__ void pack_kernel(int fmt, size_t nblk, const uint8_t* __restrict__ co
   if (blk >= nblk) return;
   const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(codes + 32 * blk));
   const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(codes + 32 * blk + 16));
-  const uint32_t lim = 1u << fmt;
+  const uint32_t lim = 1u << (fmt == MOEQ_FP3_PACKED24 ? 3 : fmt);
   uint32_t c[32];
   bool bad = false;
 #pragma unroll
@@ -32,6 +32,20 @@ __global__ void pack_kernel(int fmt, size_t nblk, const uint8_t* __restrict__ co
     c[j] &= lim - 1;
   }
   if (bad) set_status(status, MOEQ_ERR_DEVICE_INDEX);
+  if (fmt == MOEQ_FP3_PACKED24) {  // code j at bits 3j..3j+2 of the 96-bit block
+    uint32_t w[3] = {0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int bit = 3 * j;
+      w[bit >> 5] |= c[j] << (bit & 31);
+      if ((bit & 31) > 29) w[(bit >> 5) + 1] |= c[j] >> (32 - (bit & 31));  // the field crosses a word
+    }
+    uint32_t* o = reinterpret_cast<uint32_t*>(out + 12 * blk);
+    o[0] = w[0];
+    o[1] = w[1];
+    o[2] = w[2];
+    return;
+  }
   if (fmt == 4) {
     uint32_t w[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -68,7 +82,7 @@ using namespace moeq;
 extern "C" int moe_pack_expert(int fmt, int rows, int cols, const uint8_t* codes_u8,
                                const void* scales, void* out_codes, void* out_scales,
                                int32_t* dev_status, moeq_stream stream) {
-  if (fmt != 2 && fmt != 3 && fmt != 4) return MOEQ_ERR_FORMAT;
+  if (fmt != 2 && fmt != 3 && fmt != 4 && fmt != MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;
   if (rows < 0 || cols < 0 || cols % 32) return MOEQ_ERR_SHAPE;
   if (rows == 0 || cols == 0) return MOEQ_OK;
   if (!codes_u8 || !out_codes) return MOEQ_ERR_ARG;

@@ -271,6 +271,7 @@ extern "C" int moe_ffn_prefill(const moeq_layer* L, const uint16_t* x, int T, co
                                const moeq_debug* dbg, moeq_stream stream) {
   int rc = validate_layer(L);
   if (rc) return rc;
+  if (L->down.fmt == MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;  // decode-only layout
   if (T < 0) return MOEQ_ERR_SHAPE;
   if (T == 0) return MOEQ_OK;
   if (!x || !y) return MOEQ_ERR_ARG;
@@ -389,6 +390,7 @@ extern "C" int moe_ffn_stack_prefill(const moeq_layer* layers, int nlayers, cons
   for (int l = 0; l < nlayers; ++l) {
     const int rc = validate_layer(&layers[l]);
     if (rc) return rc;
+    if (layers[l].down.fmt == MOEQ_FP3_PACKED24) return MOEQ_ERR_FORMAT;
     if (layers[l].H != H) return MOEQ_ERR_SHAPE;
     const PrefillWs wl = prefill_ws_layout(layers[l].H, layers[l].I, layers[l].E, layers[l].k,
                                            layers[l].has_shared, T);

@@ -166,7 +166,12 @@ __global__ void rmsnorm_kernel(const float* __restrict__ r, int T, int H, uint16
 // when a is given, a = RMSNorm(r) as moe_rmsnorm_bf16.
 __global__ void stack_step_kernel(const uint16_t* __restrict__ x, const float* __restrict__ y,
                                   float* __restrict__ r, uint16_t* __restrict__ a, int H) {
+  // one warp per row of the residual stream
   const int lane = threadIdx.x & 31;
+  const size_t off = static_cast<size_t>(threadIdx.x >> 5) * H;
+  r += off;
+  if (x) x += off;
+  if (y) y += off;
   for (int k = lane; k < H; k += 32) {
     if (x) {
       r[k] = __uint_as_float(static_cast<uint32_t>(x[k]) << 16);
@@ -175,7 +180,7 @@ __global__ void stack_step_kernel(const uint16_t* __restrict__ x, const float* _
     }
   }
   __syncwarp();
-  if (a) rmsnorm_row(r, H, a, lane);
+  if (a) rmsnorm_row(r, H, a + off, lane);
 }
 
 }  // namespace
@@ -222,9 +227,10 @@ extern "C" int h32_rotate(const float* in, float* out, int nblk, const uint32_t*
   return cuda_status(cudaGetLastError());
 }
 
-// Enqueues one stack step (see stack_step_kernel).
-int moeq::stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, cudaStream_t s) {
-  stack_step_kernel<<<1, 32, 0, s>>>(x, y, r, a, H);
+// Enqueues one stack step over `rows` rows (see stack_step_kernel).
+int moeq::stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, int rows,
+                            cudaStream_t s) {
+  stack_step_kernel<<<1, 32 * rows, 0, s>>>(x, y, r, a, H);
   return cuda_status(cudaGetLastError());
 }
 

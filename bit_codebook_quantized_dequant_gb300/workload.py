@@ -45,7 +45,7 @@ class DeviceMatrix:
     def desc(self) -> MoeqMatrix:
         return MoeqMatrix(self.fmt, self.rows, self.cols, self.E, self.codes.data_ptr(),
                           self.stride_codes, self.scales.data_ptr(), self.stride_scales,
-                          self.codebooks.data_ptr(), 1 << self.fmt, CB_STRIDE)
+                          self.codebooks.data_ptr(), 1 << S.code_bits(self.fmt), CB_STRIDE)
 
     @property
     def nbytes(self) -> int:
@@ -65,14 +65,15 @@ def build_matrix(seed: int, layer: int, cfg: dict, name: str, scratch: Optional[
         scratch = torch.empty(rows * cols, dtype=torch.uint8, device=device)
     role = S.MATRIX_ROLES[name]
     nb = cols // 32
+    bits = S.code_bits(fmt)
     for e in range(E):
-        moeq_synth_codes(seed, S.stream_id(layer, role, e, S.KIND_CODES), fmt, rows * cols, scratch)
+        moeq_synth_codes(seed, S.stream_id(layer, role, e, S.KIND_CODES), bits, rows * cols, scratch)
         sp = scales.data_ptr() + e * ssb
-        moeq_synth_scales(seed, S.stream_id(layer, role, e, S.KIND_SCALES), fmt, rows * nb, sp)
+        moeq_synth_scales(seed, S.stream_id(layer, role, e, S.KIND_SCALES), bits, rows * nb, sp)
         moe_pack_expert(fmt, rows, cols, scratch, sp, codes.data_ptr() + e * scb, sp)
     books = np.zeros((E, CB_STRIDE), dtype=np.int8)  # records padded to 16 bytes
     for e in range(E):
-        books[e, : 1 << fmt] = S.codebook(seed, S.stream_id(layer, role, e, S.KIND_CODEBOOK), fmt)
+        books[e, : 1 << bits] = S.codebook(seed, S.stream_id(layer, role, e, S.KIND_CODEBOOK), bits)
     codebooks = torch.from_numpy(books).to(device)
     return DeviceMatrix(fmt, rows, cols, E, codes, scales, codebooks, scb, ssb)
 

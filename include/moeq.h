@@ -29,6 +29,9 @@
  *   FP3 block  : low two bits as FP2 in w0, w1; bit 2 of element (w, h, n) at
  *                bit 4n + p(w,h) of w2, p(0,0)=2, p(0,1)=3, p(1,0)=0, p(1,1)=1
  *   FP4 block  : element j in nibble j%8 of word j/8
+ *   FP3 Packed24 block (format code 24): the same 12 bytes and fp16 scale
+ *                as FP3, code j at bits 3j .. 3j+2 of the block read as one
+ *                96-bit little-endian integer (8 codes per 24 bits)
  *   weight     : scale(r, b) * codebook[code]
  */
 #ifndef MOEQ_H
@@ -44,10 +47,23 @@ extern "C" {
 typedef struct CUstream_st* moeq_stream; /* a cudaStream_t; NULL = legacy default stream */
 
 /* Weight formats. FP2/FP3/FP4: packed 32-weight codebook blocks (the layer
- * roles). MOEQ_BF16: unpacked bf16 rows, no scales or codebooks (the router's
- * format; no packed role takes it, moeq_packed_bytes sizes it as rows x cols
- * x 2 bytes of codes and no scale plane). */
-typedef enum { MOEQ_FP2 = 2, MOEQ_FP3 = 3, MOEQ_FP4 = 4, MOEQ_BF16 = 16 } moeq_fmt;
+ * roles). MOEQ_FP3_PACKED24: FP3 codes in the Packed24 bit order (the
+ * "Packed24 FP3" variant of "deepseek-v4-flash-0731-evox3-rocm", section "The
+ * optimization ladder", which names it only; the bit order above is this
+ * library's reading), same bytes per block as FP3, accepted for the routed
+ * down projection of the decode and q=4 entry points (and by pack, expand)
+ * and rejected with MOEQ_ERR_FORMAT elsewhere: a layout to weigh the decode's
+ * integer-pipe cost of unpacking 3-bit fields against FP3's planes.
+ * MOEQ_BF16: unpacked bf16 rows, no scales or codebooks (the router's format;
+ * no packed role takes it, moeq_packed_bytes sizes it as rows x cols x 2
+ * bytes of codes and no scale plane). */
+typedef enum {
+  MOEQ_FP2 = 2,
+  MOEQ_FP3 = 3,
+  MOEQ_FP4 = 4,
+  MOEQ_BF16 = 16,
+  MOEQ_FP3_PACKED24 = 24
+} moeq_fmt;
 
 typedef enum {
   MOEQ_OK = 0,
@@ -149,8 +165,9 @@ int moeq_validate_layer(const moeq_layer* L);
 
 /* Workspace bytes for a call: mode 0 = decode, 1 = q=4 verify, 2 = prefill of
  * up to T_max tokens, 3 = moe_ffn_stack_prefill of up to T_max tokens through
- * layers shaped like L, 4 = moe_ffn_stack_decode through layers shaped like L
- * (T_max is ignored for modes 0, 1 and 4). 0 on an invalid descriptor. */
+ * layers shaped like L, 4 = moe_ffn_stack_decode through layers shaped like L,
+ * 5 = moe_ffn_stack_verify_q4 through layers shaped like L (T_max is ignored
+ * for modes 0, 1, 4 and 5). 0 on an invalid descriptor. */
 size_t moe_ffn_workspace(const moeq_layer* L, int T_max, int mode);
 
 /* Zero a freshly allocated workspace (enqueued memset). Needed once; every
@@ -163,15 +180,16 @@ int moe_ffn_workspace_init(void* ws, size_t ws_bytes, moeq_stream stream);
  * up to 32 tok/s on AMD Ryzen AI MAX+ 395", section "ROCmFPX: fitting 284B
  * weights into 128 GB" (blocks of 32 weights stored as small codebook codes
  * with one small scale each; FP2 2.5, FP3 3.5, FP4 4.25 bits per weight):
- * codes_u8 [rows x cols] (one code per byte, < 2^fmt) and scales
+ * codes_u8 [rows x cols] (one code per byte, below 2^bits) and scales
  * [rows x cols/32] (fp16 bits for FP2/FP3, E8M0 bytes for FP4, row-major) go
  * to the code plane out_codes (per 32-block: FP2 8 bytes of 2-bit codes, FP3
  * 12 bytes: the low two bits of the codes in two words and their third bits in
- * a third, FP4 16 bytes of nibbles)
- * and the scale plane out_scales (the input's layout; it is copied). fmt is 2,
- * 3 or 4 (MOEQ_ERR_FORMAT otherwise); cols % 32 == 0; all pointers are device
- * pointers owned by the caller, 16-byte aligned. A code out of range sets
- * *dev_status to MOEQ_ERR_DEVICE_INDEX and is packed masked to fmt bits. */
+ * a third, FP3 Packed24 12 bytes of consecutive 3-bit fields, FP4 16 bytes of
+ * nibbles) and the scale plane out_scales (the input's layout; it is copied).
+ * fmt is 2, 3, 4 or MOEQ_FP3_PACKED24 (MOEQ_ERR_FORMAT otherwise); cols % 32
+ * == 0; all pointers are device pointers owned by the caller, 16-byte aligned.
+ * A code out of range sets *dev_status to MOEQ_ERR_DEVICE_INDEX and is packed
+ * masked to the format's bits. */
 int moe_pack_expert(int fmt, int rows, int cols, const uint8_t* codes_u8, const void* scales,
                     void* out_codes, void* out_scales, int32_t* dev_status, moeq_stream stream);
 
@@ -214,14 +232,17 @@ int moe_quantize_expert(int fmt, int rows, int cols, const float* w, uint8_t* co
  * moe_ffn_decode_expanded: batch-1 decode of a layer whose gate, up, down
  * (and shared) matrices are MOEQ_BF16 rows (codes = bf16 [rows x cols] per
  * expert, expert_stride_codes bytes apart; scales and codebooks unused): the
- * router and top-k of moe_route_topk, then per slot g = W_gate x, u = W_up x
- * (bf16 weights, x as given, fp32 sums), h = silu(g) u in fp32 (no
+ * router logits, top-k and weights of moe_route_topk (the same canonical
+ * order, one warp per router row over the grid), then per slot g = W_gate x,
+ * u = W_up x (bf16 weights, x as given, fp32 sums), h = silu(g) u in fp32 (no
  * quantization), o = W_down h, y = sum_slot p o + o_shared in slot order.
  * H a multiple of 256, I of 128, E <= 1024, no H32 rotation. ws: at least
- * moe_ffn_expanded_workspace(H, I, k, has_shared) bytes of device memory.
+ * moe_ffn_expanded_workspace(H, I, E, k, has_shared) bytes of device memory,
+ * zeroed once (each call leaves its arrival counter at zero); layout idx
+ * [k] int32 at byte 0, then p, the counter, logits and h, 256-byte aligned.
  * Three kernels enqueued on the stream. */
 int moe_expand_bf16(const moeq_matrix* m, int e0, int ne, uint16_t* out_bf16, moeq_stream stream);
-size_t moe_ffn_expanded_workspace(int H, int I, int k, int has_shared);
+size_t moe_ffn_expanded_workspace(int H, int I, int E, int k, int has_shared);
 int moe_ffn_decode_expanded(const moeq_layer* L, const uint16_t* x, float* y, void* ws, size_t ws_bytes,
                             int32_t* dev_status, moeq_stream stream);
 
@@ -337,6 +358,21 @@ int moe_ffn_stack_prefill(const moeq_layer* layers, int nlayers, const uint16_t*
  * synchronization; the shapes each decode takes are those of moe_ffn_decode. */
 int moe_ffn_stack_decode(const moeq_layer* layers, int nlayers, const uint16_t* x, float* r,
                          void* ws, size_t ws_bytes, int32_t* dev_status, moeq_stream stream);
+
+/* q=4 verification through a stack of nlayers layers: four independently
+ * routed columns ("DeepSeek V4 Flash: 284B model ...", section "Decode: up to
+ * 32 tok/s": every packed weight a call touches is decoded once for all the
+ * columns that use it), each carried through the layers with the recurrence
+ * of moe_ffn_stack_decode:
+ *   r_0[c] = float(x[c]);  a_l[c] = RMSNorm(r_l[c]);  r_{l+1}[c] = r_l[c] + y_l[c]
+ * with y_l = moe_ffn_verify_q4 of layer l on the four a_l (no dense
+ * projection). Column c of r_nlayers equals moe_ffn_stack_decode of x[c] bit
+ * for bit. x [4 x H] bf16; r [4 x H] fp32 receives r_nlayers. ws: at least
+ * moe_ffn_workspace(L, 1, 5) bytes for the largest layer shape, zeroed once
+ * with moe_ffn_workspace_init. 2 * nlayers + 1 kernels enqueued on the
+ * stream, no host synchronization; shapes as for moe_ffn_verify_q4. */
+int moe_ffn_stack_verify_q4(const moeq_layer* layers, int nlayers, const uint16_t* x, float* r,
+                            void* ws, size_t ws_bytes, int32_t* dev_status, moeq_stream stream);
 
 /* H32 rotation ("deepseek-v4-flash-0731-evox3-rocm", section "The optimization
  * ladder"): out = H D in per 32-block, H the 32x32 Sylvester Hadamard matrix

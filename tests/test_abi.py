@@ -51,7 +51,7 @@ def _mat(fmt, rows, cols, E, **kw):
     cb, sb = M.moeq_packed_bytes(fmt, rows, cols)
     d = dict(fmt=fmt, rows=rows, cols=cols, num_experts=E, codes=FAKE, expert_stride_codes=cb,
              scales=FAKE, expert_stride_scales=(sb + 15) // 16 * 16, codebooks=FAKE,
-             cb_len=1 << fmt, cb_stride=16)
+             cb_len=1 << (3 if fmt == M.MOEQ_FP3_PACKED24 else fmt), cb_stride=16)
     d.update(kw)
     return M.MoeqMatrix(**d)
 
@@ -141,8 +141,43 @@ def test_entry_points_reject_bad_arguments_before_launch():
     assert lib.moe_ffn_stack_decode(arr, 2, FAKE, FAKE, FAKE, need_s - 16, None, None) == \
         M.CODE["MOEQ_ERR_WORKSPACE"]
     assert lib.moe_ffn_stack_decode(arr, 2, FAKE + 8, FAKE, FAKE, need_s, None, None) == M.CODE["MOEQ_ERR_ALIGN"]
+    # q=4 stack: q=4 workspace + a [4 x H] + y [4 x H] for the largest layer
+    assert lib.moe_ffn_stack_verify_q4(None, 1, FAKE, FAKE, FAKE, 1 << 30, None, None) == M.CODE["MOEQ_ERR_ARG"]
+    need_q = lib.moe_ffn_workspace(C.byref(L), 1, 5)
+    assert need_q == need4 + 8 * L.H + 16 * L.H
+    assert lib.moe_ffn_stack_verify_q4(arr, 2, FAKE, FAKE, FAKE, need_q - 16, None, None) == \
+        M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert lib.moe_ffn_stack_verify_q4(arr, 2, FAKE, FAKE + 4, FAKE, need_q, None, None) == \
+        M.CODE["MOEQ_ERR_ALIGN"]
+    other = (M.MoeqLayer * 2)(L, _layer(H=2 * L.H))
+    assert lib.moe_ffn_stack_verify_q4(other, 2, FAKE, FAKE, FAKE, 1 << 30, None, None) != M.CODE["MOEQ_OK"]
     assert lib.h32_rotate(None, None, 4, None, None) == M.CODE["MOEQ_ERR_ARG"]
     assert lib.moe_rmsnorm_bf16(FAKE, 1, 100, FAKE, None) == M.CODE["MOEQ_ERR_SHAPE"]
+
+
+def test_packed24_layout_accepted_for_routed_down_only():
+    P24 = M.MOEQ_FP3_PACKED24
+    assert M.moeq_packed_bytes(P24, 4096, 2048) == M.moeq_packed_bytes(3, 4096, 2048)
+    assert M.moeq_validate_layer(_layer(down=_mat(P24, 256, 256, 16))) == 0
+    assert M.moeq_validate_layer(_layer(down=_mat(P24, 256, 256, 16, cb_len=16))) == \
+        M.CODE["MOEQ_ERR_CODEBOOK_MISMATCH"]
+    assert M.moeq_validate_layer(_layer(gate=_mat(P24, 256, 256, 16), up=_mat(P24, 256, 256, 16))) == \
+        M.CODE["MOEQ_ERR_FORMAT"]
+    sh = _layer(has_shared=1, sgate=_mat(4, 256, 256, 1), sup=_mat(4, 256, 256, 1),
+                sdown=_mat(P24, 256, 256, 1))
+    assert M.moeq_validate_layer(sh) == M.CODE["MOEQ_ERR_FORMAT"]
+    lib = M.load()
+    L = _layer(down=_mat(P24, 256, 256, 16))
+    need = lib.moe_ffn_workspace(C.byref(L), 8, 2)
+    # the prefill's tensor-core GEMM does not decode the layout: rejected before any launch
+    assert lib.moe_ffn_prefill(C.byref(L), FAKE, 8, None, FAKE, FAKE, need, None, None, None) == \
+        M.CODE["MOEQ_ERR_FORMAT"]
+    assert lib.moe_ffn_stack_prefill((M.MoeqLayer * 1)(L), 1, FAKE, 8, FAKE, FAKE, 1 << 40, None, None) == \
+        M.CODE["MOEQ_ERR_FORMAT"]
+    # nor does the q=4 dense projection
+    dense = _mat(P24, 256, 256, 1)
+    assert lib.moe_ffn_verify_q4(C.byref(_layer()), C.byref(dense), FAKE, FAKE, FAKE, FAKE, 1 << 30, None,
+                                 None, None) == M.CODE["MOEQ_ERR_FORMAT"]
 
 
 def test_prefill_entry_points_reject_bad_arguments_before_launch():

@@ -33,10 +33,12 @@ def test_generator_twin_matches_host(bits):
 
 
 @pytest.mark.parametrize("fmt,rows,cols", [(2, 2048, 4096), (3, 4096, 2048), (4, 2048, 4096),
-                                           (2, 3, 128), (3, 5, 256), (4, 1, 128)])
+                                           (24, 4096, 2048), (2, 3, 128), (3, 5, 256), (4, 1, 128),
+                                           (24, 5, 256)])
 def test_pack_bit_exact(fmt, rows, cols):
-    codes = S.codes(5, fmt * 1000 + rows, fmt, rows, cols)
-    scales = S.scales(5, fmt * 1000 + rows + 1, fmt, rows * cols // 32)
+    bits = S.code_bits(fmt)
+    codes = S.codes(5, fmt * 1000 + rows, bits, rows, cols)
+    scales = S.scales(5, fmt * 1000 + rows + 1, bits, rows * cols // 32)
     cbytes, sbytes = M.moeq_packed_bytes(fmt, rows, cols)
     d_codes = torch.from_numpy(codes).cuda()
     d_scales = torch.from_numpy(scales.view(np.uint8)).cuda()

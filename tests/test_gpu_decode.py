@@ -75,9 +75,10 @@ def test_decode_config1_sampled_tokens():
         check_token(L, cfg, xs[t], y, g, partials=(t == 0))
 
 
-@pytest.mark.parametrize("name", ["decode-b1-top4", "decode-b1-fp2down"])
+@pytest.mark.parametrize("name", ["decode-b1-top4", "decode-b1-fp2down", "decode-b1-p24down"])
 def test_decode_format_variants(name):
-    # top-4 routing, and FP2 down projections, on the decode layer's shape
+    # top-4 routing, FP2 down projections, and FP3 down projections in the
+    # Packed24 layout, on the decode layer's shape
     cfg = _cfg(name)
     seed = S.workload_seed(name)
     dl = build_layer(seed, 0, cfg)
@@ -87,6 +88,35 @@ def test_decode_format_variants(name):
     for t in range(xs.shape[0]):
         y, g = _run(dl, ws, xs[t], partials=(t == 0))
         check_token(L, cfg, xs[t], y, g, partials=(t == 0))
+
+
+def test_packed24_down_equals_fp3_down_bit_for_bit():
+    """The same codes, scales and codebooks with the down projections in the
+    Packed24 layout instead of FP3's planes: decode and q=4 give the same y bit
+    for bit (the layout changes only how the codes are unpacked)."""
+    cfg3 = _cfg("decode-b1")
+    cfg24 = dict(cfg3, fmt_down=24)
+    seed = S.workload_seed("decode-b1")
+    d3, d24 = build_layer(seed, 1, cfg3), build_layer(seed, 1, cfg24)
+    assert d24.desc().down.fmt == 24
+    H = cfg3["H"]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    xs = S.tokens(seed, cfg3, 8, start=300)
+    for mode, T in ((0, 1), (1, 4)):
+        w3, w24 = Workspace(d3, mode), Workspace(d24, mode)
+        for b in range(0, 8, T):
+            x = to_dev_u16(xs[b:b + T] if T > 1 else xs[b])
+            ys = []
+            for dl, ws in ((d3, w3), (d24, w24)):
+                y = torch.zeros(T * H, dtype=torch.float32, device="cuda")
+                if T == 1:
+                    M.moe_ffn_decode(dl.desc(), x, y, ws.ptr, ws.nbytes, st)
+                else:
+                    M.moe_ffn_verify_q4(dl.desc(), None, x, y, None, ws.ptr, ws.nbytes, st)
+                torch.cuda.synchronize()
+                assert st.item() == 0
+                ys.append(y.cpu().numpy())
+            np.testing.assert_array_equal(ys[1], ys[0])
 
 
 def test_decode_repeatable_and_workspace_reused():

@@ -65,7 +65,7 @@ def test_expanded_decode_against_fp64_definition(name):
             ref = torch.from_numpy(_dense_bf16(m, e).astype(np.float32)).to(torch.bfloat16)
             np.testing.assert_array_equal(got, ref.view(torch.int16).numpy().view(np.uint16).ravel(),
                                           err_msg=f"{n} expert {e}")
-    ws_bytes = M.moe_ffn_expanded_workspace(H, cfg["I"], cfg["k"], 1 if cfg["shared_fmt"] else 0)
+    ws_bytes = M.moe_ffn_expanded_workspace(H, cfg["I"], cfg["E"], cfg["k"], 1 if cfg["shared_fmt"] else 0)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     for t in range(xs.shape[0]):

@@ -80,3 +80,32 @@ def test_stack_decode_matches_composition_and_oracle():
             f"token {t}: max err/B {np.max(err / bound):.3g}"
         checked += 1
     assert checked >= 2
+
+
+def test_stack_verify_q4_columns_equal_stack_decode():
+    """Four columns through the stack with moe_ffn_stack_verify_q4 (each layer's
+    weights read once per call for all columns) equal, column by column and bit
+    for bit, moe_ffn_stack_decode of each column, which the test above pins to
+    the oracle; columns 1 and 3 are equal, so some units serve two columns."""
+    cfg = dict(S.WORKLOADS["prefill-43-layer-stack"])
+    seed = S.workload_seed("prefill-43-layer-stack")
+    layers = [build_layer(seed, l, cfg) for l in range(NL)]
+    descs = [dl.desc() for dl in layers]
+    H = cfg["H"]
+    X = S.tokens(seed, cfg, 3, start=950)
+    X4 = np.stack([X[0], X[1], X[2], X[1]])
+    ws4 = Workspace(layers[0], 5)
+    ws1 = Workspace(layers[0], 4)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x4 = to_dev_u16(X4)
+    r4 = torch.zeros(4, H, dtype=torch.float32, device="cuda")
+    for _ in range(2):  # the second call on the same workspace must repeat the first
+        M.moe_ffn_stack_verify_q4(descs, x4, r4, ws4.ptr, ws4.nbytes, st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        for c in range(4):
+            r1 = torch.zeros(H, dtype=torch.float32, device="cuda")
+            M.moe_ffn_stack_decode(descs, to_dev_u16(X4[c]), r1, ws1.ptr, ws1.nbytes, st)
+            torch.cuda.synchronize()
+            assert st.item() == 0
+            np.testing.assert_array_equal(r4[c].cpu().numpy(), r1.cpu().numpy())
