@@ -96,6 +96,18 @@ def source_sha(source: str) -> str:
     return h.hexdigest()[:16]
 
 
+# Target fractions of each path's roofline (the decode and q=4 lines: 70 % of
+# HBM; the tensor-core-bound prefill: 50 % of the bf16 peak).
+TARGET_HBM, TARGET_TC = 0.70, 0.50
+
+
+def _target(roof: dict, target):
+    """The target fraction and the gap to it, beside the achieved fraction."""
+    roof["target_frac"] = target
+    roof["gap_to_target"] = None if target is None else target - roof["frac"]
+    return roof
+
+
 def _traffic(kernel: str, source: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current source of the kernel (its file and the device header); else
@@ -488,6 +500,7 @@ def bench_verify(args, hbm_peak, peak_kind, cpu=False):
                         "algorithmic_bytes_per_launch": per_call},
            "gpu_launches": steps, "launch": "CUDA graph replay",
            "parity_after": parity}
+    _target(out["roofline"], TARGET_HBM)
     del layers, wss
     torch.cuda.empty_cache()
     return out
@@ -569,6 +582,8 @@ def bench_prefill(args, name, T, tc_peak, hbm_peak, peak_kind, cpu=False):
     # the layer's bound: its FLOP per weight byte against the bf16 ridge
     ridge = tc_peak * 1e12 / (hbm_peak * 1e9)
     hbm_bound = fl / wbytes < ridge
+    _target(tensor, TARGET_TC)
+    _target(hbm, None)  # no HBM target is stated for the prefill
     out = {"metric": "prefill tok/s (one layer)", "value": T / (ms * 1e-3), "unit": "tok/s",
            "ms_per_call": ms, "calls": steps, "tokens": T,
            "workload": name + f": T={T}, one layer, all 256 experts' weights read once",
@@ -636,9 +651,12 @@ def bench_stack(args, T, nlayers, tc_peak, peak_kind):
                                      "teacher-forced per layer) is a GPU test"}}
     del ws, r, r1
     torch.cuda.empty_cache()
+    _target(out["roofline"], TARGET_TC)
     dec = bench_stack_decode(args, layers, cfg, seed)
+    _target(dec["roofline"], TARGET_HBM)
     torch.cuda.empty_cache()
     dec["verify_q4_stack"] = bench_stack_verify(args, layers, cfg, seed)
+    _target(dec["verify_q4_stack"]["roofline"], TARGET_HBM)
     del layers
     torch.cuda.empty_cache()
     return out, dec
@@ -1104,6 +1122,7 @@ def run(args):
         "cpu_baseline": cpu,
         "parity_after": parity_after,
     }
+    _target(line["roofline"], TARGET_HBM)
     line.update(extra)
     print(json.dumps(line))
     if dist:

@@ -1151,6 +1151,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const DecodeArgs a) {
 
   // ---------------------------------------------------------------- teardown
   __syncthreads();
+  int ntd = 0;  // teardown trace events (role 2, thread 0)
+  if (tid == 0) trace_ev(a, 2, ntd, MOEQ_TRACE_START, 0);
   if (warp == kProducerWarp && lane == 0) {
     // fills issued but never waited for (only after a timeout): let them land
     for (int g = 0; g < kGroups; ++g)
@@ -1167,6 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const DecodeArgs a) {
       const uint32_t target = static_cast<uint32_t>(a.nSD + sm.nu * per);
       if (lane == 0 && !spin_until_geq(&a.ctr[kCtrDownDone], target, a.spin))
         set_status(a.status, MOEQ_ERR_DEVICE_TIMEOUT);
+      if (lane == 0) trace_ev(a, 2, ntd, MOEQ_TRACE_READY, 0);
       __syncwarp();
     }
     __syncthreads();
@@ -1180,11 +1183,14 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const DecodeArgs a) {
       if (a.has_shared) acc += __ldcg(&a.obuf[(static_cast<size_t>(a.su) * COLS + c) * a.H + row]);
       a.y[static_cast<size_t>(c) * a.H + row] = acc;
     }
+    __syncthreads();
+    if (tid == 0) trace_ev(a, 2, ntd, MOEQ_TRACE_DONE, 0);
   }
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     const uint32_t old = atomicAdd(&a.ctr[kCtrDone], 1u);
+    trace_ev(a, 2, ntd, MOEQ_TRACE_EPI_END, static_cast<int>(old));
     sm.last_cta = old == gridDim.x - 1;
     if (sm.last_cta) __threadfence();
   }

@@ -135,7 +135,10 @@ typedef struct {
 } moeq_debug;
 
 /* Timeline events of moe_ffn_decode and moe_ffn_verify_q4 (role 0 = compute
- * group 0, 1 = producer warp, 3 = compute group 1; role 2 is not used).
+ * group 0, 1 = producer warp, 3 = compute group 1, 2 = the CTA's teardown:
+ * START when its compute ended, READY when the wait for every down item
+ * passed, DONE when its combined rows of y are written (CTAs that combine),
+ * EPI_END at its arrival on the done counter, unit = arrivals before it).
  * Unused entries stay as the caller left them. */
 enum {
   MOEQ_TRACE_START = 1,      /* compute: x quantized; producer: first unit taken */
