@@ -1177,10 +1177,17 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const DecodeArgs a) {
     if (cc < nchunks) {
       const int c = cc / per;
       const int row = (cc % per) * kDownRows + lane;
+      // every slot's output in flight at once, then summed in slot order
+      float v[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        v[j] = j < a.k ? __ldcg(&a.obuf[(static_cast<size_t>(sm.uof[c][j]) * COLS + c) * a.H + row]) : 0.0f;
+      const float vs = a.has_shared ? __ldcg(&a.obuf[(static_cast<size_t>(a.su) * COLS + c) * a.H + row]) : 0.0f;
       float acc = 0.0f;
-      for (int j = 0; j < a.k; ++j)
-        acc = fmaf(sm.p[c][j], __ldcg(&a.obuf[(static_cast<size_t>(sm.uof[c][j]) * COLS + c) * a.H + row]), acc);
-      if (a.has_shared) acc += __ldcg(&a.obuf[(static_cast<size_t>(a.su) * COLS + c) * a.H + row]);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < a.k) acc = fmaf(sm.p[c][j], v[j], acc);
+      if (a.has_shared) acc += vs;
       a.y[static_cast<size_t>(c) * a.H + row] = acc;
     }
     __syncthreads();
