@@ -88,7 +88,7 @@ struct TcGemm {
 int tc_grouped_gemm(const TcGemm& g, cudaStream_t s);
 
 // One step of a decode stack on `rows` tokens (route.cu), row by row: r =
-// float(x) if x, else r += y if y; then a = RMSNorm(r) if a. One warp a row.
+// float(x) if x, else r += y if y; then a = RMSNorm(r) if a. One CTA a row.
 int stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, int rows,
                       cudaStream_t s);
 

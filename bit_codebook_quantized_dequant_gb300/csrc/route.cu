@@ -125,7 +125,10 @@ __global__ void h32_kernel(const float* __restrict__ in, float* out, int nblk,
 
 // RMSNorm of one row by one warp: sum of squares in the canonical order,
 // correctly rounded fp32 steps, then a = bf16_rne(r * inv).
-__device__ __forceinline__ void rmsnorm_row(const float* row, int H, uint16_t* out, int lane) {
+// 1 / sqrt(mean(row^2) + 1e-6) of one row by one warp: the sum of squares in
+// the router's canonical order (lane j over h = 256 i + 8 j + t, each square
+// rounded, then the combining rounds), each step correctly rounded.
+__device__ __forceinline__ float rms_inv(const float* row, int H, int lane) {
   float s = 0.0f;
   for (int i = 0; i < H / 256; ++i) {
     const float4 v0 = *reinterpret_cast<const float4*>(row + 256 * i + 8 * lane);
@@ -141,7 +144,11 @@ __device__ __forceinline__ void rmsnorm_row(const float* row, int H, uint16_t* o
   }
   s = warp_sum_canonical(s);
   const float ms = __fdiv_rn(s, static_cast<float>(H));
-  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, 1e-6f)));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, 1e-6f)));
+}
+
+__device__ __forceinline__ void rmsnorm_row(const float* row, int H, uint16_t* out, int lane) {
+  const float inv = rms_inv(row, H, lane);
   for (int k0 = 8 * lane; k0 < H; k0 += 256) {
     const float4 v0 = *reinterpret_cast<const float4*>(row + k0);
     const float4 v1 = *reinterpret_cast<const float4*>(row + k0 + 4);
@@ -161,26 +168,42 @@ __global__ void rmsnorm_kernel(const float* __restrict__ r, int T, int H, uint16
   rmsnorm_row(r + static_cast<size_t>(t) * H, H, a + static_cast<size_t>(t) * H, lane);
 }
 
-// One step of a decode stack on one token (one warp): r = float(x) when x is
-// given, else r = r + y when y is given (correctly rounded fp32 adds); then,
-// when a is given, a = RMSNorm(r) as moe_rmsnorm_bf16.
-__global__ void stack_step_kernel(const uint16_t* __restrict__ x, const float* __restrict__ y,
-                                  float* __restrict__ r, uint16_t* __restrict__ a, int H) {
-  // one warp per row of the residual stream
-  const int lane = threadIdx.x & 31;
-  const size_t off = static_cast<size_t>(threadIdx.x >> 5) * H;
+// One step of a decode stack, one CTA per row of the residual stream: r =
+// float(x) when x is given, else r = r + y when y is given (correctly rounded
+// fp32 adds), by every thread with all loads in flight; then, when a is given,
+// a = RMSNorm(r) with rmsnorm_row's arithmetic (its sum of squares by warp 0 in
+// the canonical order, from a shared-memory copy of the row), so a equals
+// moe_rmsnorm_bf16 of r bit for bit.
+constexpr int kStepThreads = 512;
+
+__global__ void __launch_bounds__(kStepThreads) stack_step_kernel(const uint16_t* __restrict__ x,
+                                                                   const float* __restrict__ y,
+                                                                   float* __restrict__ r, uint16_t* __restrict__ a,
+                                                                   int H) {
+  extern __shared__ __align__(16) float rs[];  // the row after the step [H]
+  __shared__ float inv_s;
+  const size_t off = static_cast<size_t>(blockIdx.x) * H;
   r += off;
   if (x) x += off;
   if (y) y += off;
-  for (int k = lane; k < H; k += 32) {
-    if (x) {
-      r[k] = __uint_as_float(static_cast<uint32_t>(x[k]) << 16);
-    } else if (y) {
-      r[k] = __fadd_rn(r[k], y[k]);
-    }
+  for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    float v;
+    if (x) v = __uint_as_float(static_cast<uint32_t>(x[k]) << 16);
+    else if (y) v = __fadd_rn(r[k], y[k]);
+    else v = r[k];
+    if (x || y) r[k] = v;
+    rs[k] = v;
   }
-  __syncwarp();
-  if (a) rmsnorm_row(r, H, a + off, lane);
+  __syncthreads();
+  if (!a) return;
+  if (threadIdx.x < 32) {
+    const float inv = rms_inv(rs, H, threadIdx.x);
+    if (threadIdx.x == 0) inv_s = inv;
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  a += off;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) a[k] = f32_to_bf16_rne(__fmul_rn(rs[k], inv));
 }
 
 }  // namespace
@@ -230,7 +253,7 @@ extern "C" int h32_rotate(const float* in, float* out, int nblk, const uint32_t*
 // Enqueues one stack step over `rows` rows (see stack_step_kernel).
 int moeq::stack_step_launch(const uint16_t* x, const float* y, float* r, uint16_t* a, int H, int rows,
                             cudaStream_t s) {
-  stack_step_kernel<<<1, 32 * rows, 0, s>>>(x, y, r, a, H);
+  stack_step_kernel<<<rows, kStepThreads, static_cast<size_t>(H) * 4, s>>>(x, y, r, a, H);
   return cuda_status(cudaGetLastError());
 }
 
