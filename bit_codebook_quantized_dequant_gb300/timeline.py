@@ -85,6 +85,27 @@ def summarize(rel, ev, unit, valid) -> list:
     for k in sorted(ready):
         stats(f"READY {KIND.get(k, k)}", ready[k])
         stats(f"DONE  {KIND.get(k, k)}", done.get(k, []))
+    # per fill kind: compute time (DONE - READY of the same fill) and the
+    # group's idle gap before it (READY - the group's previous DONE)
+    busy, idle = {}, {}
+    for b in range(rel.shape[0]):
+        for role in (ROLE_GROUP0, ROLE_GROUP1):
+            prev_done, ready_at = None, None
+            for i in range(rel.shape[2]):
+                if not valid[b, role, i]:
+                    continue
+                k = int((unit[b, role, i] >> 28) & 15)
+                if ev[b, role, i] == EV_READY:
+                    ready_at = rel[b, role, i]
+                    if prev_done is not None:
+                        idle.setdefault(k, []).append(ready_at - prev_done)
+                elif ev[b, role, i] == EV_DONE and ready_at is not None:
+                    busy.setdefault(k, []).append(rel[b, role, i] - ready_at)
+                    prev_done = rel[b, role, i]
+    for k in sorted(busy):
+        stats(f"compute time per fill {KIND.get(k, k)}", busy[k])
+    for k in sorted(idle):
+        stats(f"group idle before a fill {KIND.get(k, k)}", idle[k])
     m = valid[:, ROLE_TEARDOWN]
     e = ev[:, ROLE_TEARDOWN]
     stats("teardown entered (compute ended)", rel[:, ROLE_TEARDOWN][m & (e == EV_START)])
