@@ -223,3 +223,60 @@ def test_prefill_entry_points_reject_bad_arguments_before_launch():
     assert stack(r=None) == M.CODE["MOEQ_ERR_ARG"]
     assert stack(x=FAKE + 2) == M.CODE["MOEQ_ERR_ALIGN"]
     assert stack(ws_bytes=need3 - 1) == M.CODE["MOEQ_ERR_WORKSPACE"]
+
+
+def test_quantizer_and_expansion_reject_bad_arguments_before_launch():
+    lib = M.load()
+    # moe_quantize_expert: fmt 2, 3 or 4; cols % 32; pointers; alignment; >= 1 KiB of workspace
+    def quant(fmt=2, rows=4, cols=64, w=FAKE, codes=FAKE, scales=FAKE, cb=FAKE, ws=FAKE, ws_bytes=1024):
+        return lib.moe_quantize_expert(fmt, rows, cols, w, codes, scales, cb, ws, ws_bytes, None, None)
+
+    assert quant(fmt=5) == M.CODE["MOEQ_ERR_FORMAT"]
+    assert quant(fmt=M.MOEQ_FP3_PACKED24) == M.CODE["MOEQ_ERR_FORMAT"]   # a layout, not a code width
+    assert quant(cols=100) == M.CODE["MOEQ_ERR_SHAPE"]
+    assert quant(rows=0) == M.CODE["MOEQ_ERR_SHAPE"]
+    assert quant(rows=1 << 16, cols=1 << 15) == M.CODE["MOEQ_ERR_SHAPE"]  # 2^31 weights
+    assert quant(w=None) == M.CODE["MOEQ_ERR_ARG"]
+    assert quant(cb=None) == M.CODE["MOEQ_ERR_ARG"]
+    assert quant(w=FAKE + 4) == M.CODE["MOEQ_ERR_ALIGN"]
+    assert quant(ws_bytes=1019) == M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert quant(ws=None) == M.CODE["MOEQ_ERR_WORKSPACE"]
+    # moe_expand_bf16: a packed matrix, an expert range inside it, an aligned output
+    m = _mat(2, 256, 256, 16)
+    assert lib.moe_expand_bf16(None, 0, 1, FAKE, None) == M.CODE["MOEQ_ERR_ARG"]
+    assert lib.moe_expand_bf16(C.byref(m), 0, 1, None, None) == M.CODE["MOEQ_ERR_ARG"]
+    bad = M.MoeqMatrix(5, 256, 256, 16, FAKE, 1 << 20, FAKE, 1 << 20, FAKE, 32, 32)
+    assert lib.moe_expand_bf16(C.byref(bad), 0, 1, FAKE, None) == M.CODE["MOEQ_ERR_FORMAT"]
+    assert lib.moe_expand_bf16(C.byref(m), 10, 7, FAKE, None) == M.CODE["MOEQ_ERR_ARG"]
+    assert lib.moe_expand_bf16(C.byref(m), -1, 1, FAKE, None) == M.CODE["MOEQ_ERR_ARG"]
+    assert lib.moe_expand_bf16(C.byref(m), 0, 1, FAKE + 2, None) == M.CODE["MOEQ_ERR_ALIGN"]
+    assert lib.moe_expand_bf16(C.byref(m), 3, 0, FAKE, None) == 0   # nothing to expand
+    # moe_ffn_expanded_workspace: idx, p, the arrival counter, logits [E], h [(k + shared) x I]
+    need = lib.moe_ffn_expanded_workspace(4096, 2048, 256, 6, 1)
+    assert need == 3 * 256 + 1024 + 7 * 2048 * 4
+    assert lib.moe_ffn_expanded_workspace(4096, 2048, 0, 6, 1) == 0
+    assert lib.moe_ffn_expanded_workspace(4096, 2048, 4, 6, 1) == 0    # k > E
+    assert lib.moe_ffn_expanded_workspace(4096, 2048, 2048, 6, 1) == 0  # E > 1024
+
+    # moe_ffn_decode_expanded: MOEQ_BF16 matrices of the layer's shapes, no rotation
+    def bf(rows, cols, E):
+        return M.MoeqMatrix(M.MOEQ_BF16, rows, cols, E, FAKE, 2 * rows * cols, None, 0, None, 0, 0)
+
+    L = _layer(gate=bf(256, 256, 16), up=bf(256, 256, 16), down=bf(256, 256, 16))
+    wsb = lib.moe_ffn_expanded_workspace(256, 256, 16, 2, 0)
+
+    def dec(layer=L, x=FAKE, y=FAKE, ws=FAKE, ws_bytes=wsb):
+        return lib.moe_ffn_decode_expanded(C.byref(layer), x, y, ws, ws_bytes, None, None)
+
+    assert lib.moe_ffn_decode_expanded(None, FAKE, FAKE, FAKE, wsb, None, None) == M.CODE["MOEQ_ERR_ARG"]
+    assert dec(x=None) == M.CODE["MOEQ_ERR_ARG"]
+    assert dec(layer=_layer(H=200, gate=bf(256, 200, 16), up=bf(256, 200, 16), down=bf(200, 256, 16))) == \
+        M.CODE["MOEQ_ERR_SHAPE"]
+    assert dec(layer=_layer(gate=bf(256, 256, 16), up=bf(256, 256, 16), down=bf(256, 256, 16),
+                            h32_signs_x=FAKE)) == M.CODE["MOEQ_ERR_FORMAT"]
+    assert dec(layer=_layer()) == M.CODE["MOEQ_ERR_FORMAT"]            # packed matrices
+    assert dec(layer=_layer(gate=bf(256, 256, 16), up=bf(128, 256, 16), down=bf(256, 256, 16))) == \
+        M.CODE["MOEQ_ERR_SHAPE"]
+    assert dec(y=FAKE + 4) == M.CODE["MOEQ_ERR_ALIGN"]
+    assert dec(ws_bytes=wsb - 1) == M.CODE["MOEQ_ERR_WORKSPACE"]
+    assert dec(ws=None) == M.CODE["MOEQ_ERR_WORKSPACE"]
