@@ -430,7 +430,7 @@ def verify_parity_after(dl, ws, X, cfg, seed):
 
 def bench_verify(args, hbm_peak, peak_kind, cpu=False):
     """q=4 verification: 4 columns per call through moe_ffn_verify_q4, cycling
-    over 2 seeded layer replicas (each with its dense projection)."""
+    over --replicas seeded layer replicas (each with its dense projection)."""
     import torch
     import bit_codebook_quantized_dequant_gb300 as M
     from bit_codebook_quantized_dequant_gb300 import synth as S
@@ -438,7 +438,7 @@ def bench_verify(args, hbm_peak, peak_kind, cpu=False):
     name = "verify-q4"
     cfg = S.WORKLOADS[name]
     seed = S.workload_seed(name)
-    R = 2
+    R = max(1, args.replicas)
     layers = [build_layer(seed, r, cfg) for r in range(R)]
     wss = [Workspace(dl, 1) for dl in layers]
     descs = [dl.desc() for dl in layers]
@@ -475,22 +475,26 @@ def bench_verify(args, hbm_peak, peak_kind, cpu=False):
     parity = None
     if cpu:
         parity = verify_parity_after(layers[0], wss[0], X[:4], cfg, seed)
-    # distinct experts per call (routing of the same columns, outside the timed region)
-    distinct = []
+    # distinct experts per timed call: the (replica, batch) pairs the timed
+    # steps used, each weighted by its count (routing outside the timed region)
+    uses = {}
+    for i in range(args.warmup, args.warmup + steps):
+        key = (i % R, i % nb)
+        uses[key] = uses.get(key, 0) + 1
     idx = torch.zeros(4 * cfg["k"], dtype=torch.int32, device="cuda")
     w = torch.zeros(4 * cfg["k"], dtype=torch.float32, device="cuda")
-    for r in range(R):
-        for b in range(nb):
-            M.moe_route_topk(xs.data_ptr() + b * 4 * H * 2, 4, layers[r].router, cfg["E"], H,
-                             cfg["k"], idx, w)
-            distinct.append(len(set(idx.cpu().tolist())))
-    nd = float(np.mean(distinct))
+    tot = 0
+    for (r, b), n in uses.items():
+        M.moe_route_topk(xs.data_ptr() + b * 4 * H * 2, 4, layers[r].router, cfg["E"], H,
+                         cfg["k"], idx, w)
+        tot += n * len(set(idx.cpu().tolist()))
+    nd = tot / steps
     per_call = algorithmic_bytes_verify(cfg, nd)
     achieved = per_call / (ms * 1e-3) / 1e9
     out = {"metric": "q=4 verification column-tokens/s", "value": 4.0 / (ms * 1e-3),
            "unit": "column-tok/s", "ms_per_call": ms, "calls": steps,
            "workload": "verify-q4: decode-b1 layer + dense 4096x4096 FP4; 4 independently routed "
-                       "columns per call; 2 replicas cycled",
+                       f"columns per call; {R} replicas cycled",
            "distinct_experts_per_call": nd,
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                         "frac": achieved / hbm_peak,
